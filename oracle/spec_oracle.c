@@ -1,0 +1,300 @@
+/*
+ * CPU oracle for verification attention in long-context speculative decoding.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path calls this code: it is
+ * used by the tests, by smoke() and by the benchmark's CPU-baseline leg. It
+ * shares no code, header, table or constant with the CUDA library.
+ *
+ * Everything is the plain definition, in fp64, row by row:
+ *
+ *   oracle_select   the hybrid verification-set selection of Dustin
+ *                   ("Metodologia", section 1 "Aggregazione Ibrida
+ *                   dell'Attenzione"): protect an attention-sink prefix and a
+ *                   local window of recent tokens, then fill the remaining
+ *                   budget in tiers: the top-m tokens by the draft-lookahead
+ *                   score, then the most relevant remaining tokens by the
+ *                   target-historical score. Done with a full sort per tier.
+ *
+ *   oracle_attend   softmax attention of each draft-tree query over the
+ *                   concatenation [cache keys ; draft keys] with an explicit
+ *                   visibility mask. Cache keys are all tokens of the context
+ *                   (full-cache verification, Dustin "Definizione del
+ *                   Problema") or only the selected index set (Dustin
+ *                   "Workflow di Verifica", steps 3-4). Draft key j is visible
+ *                   to node i iff j == i or j is an ancestor of i in the
+ *                   draft tree (the tree mask of LongSpec section 2.C). The
+ *                   softmax is taken over everything at once: no parts, no
+ *                   splits, no merge.
+ *
+ *   oracle_lse_merge  the log-sum-exp combination of two normalised partial
+ *                   attentions (LongSpec section 2.C, "Aggregazione").
+ *
+ * Readings where the pages are silent (also listed in the design notes):
+ *   - score comparison: larger is better; -0 == +0; NaN ranks below every
+ *     number (including -inf) and NaNs tie; ties go to the lower index.
+ *   - a context of n <= budget tokens is verified in full: idx = 0..n-1,
+ *     then -1 padding.
+ *   - sink/window clip to the context: S' = min(S, n), W' = min(W, n - S').
+ *   - the top-m and fill tiers draw only from tokens outside sink and window.
+ *   - parent[i] == -1: node i hangs off the last cache token. A parent outside
+ *     [-1, i) ends the ancestor walk there and is reported as bad input.
+ *   - a sparse index entry is used iff 0 <= idx[j] < n and (j == 0 or
+ *     idx[j] > idx[j-1]); -1 entries are padding; any other unused entry is
+ *     reported as bad input.
+ *   - a row that sees no key at all has lse = -inf and o = 0.
+ *   - lse is the natural log of sum exp(scale * q.k).
+ *
+ * Return value of every function: 0 = ok, 1 = invalid argument,
+ * 5 = bad input data seen (the masked/clipped result is still written).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_INVALID_ARG 1
+#define ORACLE_BAD_INPUT 5
+
+/* bf16 bits -> exact double */
+static double bf16_to_double(uint16_t h)
+{
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* ------------------------------------------------------------------------ */
+/* selection                                                                 */
+
+typedef struct {
+    float score;
+    int32_t index;
+} scored_token;
+
+/* "a ranks before b": larger score first, NaN last, ties by lower index. */
+static int ranks_before(const scored_token *a, const scored_token *b)
+{
+    int an = isnan(a->score), bn = isnan(b->score);
+    if (an && bn) return a->index < b->index;
+    if (an) return 0;
+    if (bn) return 1;
+    if (a->score > b->score) return 1;
+    if (a->score < b->score) return 0;
+    return a->index < b->index; /* equal, including -0 == +0 */
+}
+
+static int cmp_rank(const void *pa, const void *pb)
+{
+    const scored_token *a = (const scored_token *)pa, *b = (const scored_token *)pb;
+    if (ranks_before(a, b)) return -1;
+    if (ranks_before(b, a)) return 1;
+    return 0;
+}
+
+int oracle_select(const float *draft_score, const float *target_score, int64_t ld, int B, int L,
+                  const int32_t *ctx_lens, int sink, int window, int top_m, int budget,
+                  int32_t *idx, int32_t *count)
+{
+    if (B < 0 || L < 0 || ld < L || sink < 0 || window < 0 || top_m < 0 || budget < 1 ||
+        sink + window > budget || !draft_score || !target_score || !idx)
+        return ORACLE_INVALID_ARG;
+    int status = ORACLE_OK;
+    scored_token *pool = (scored_token *)malloc(sizeof(scored_token) * (size_t)(L > 0 ? L : 1));
+    unsigned char *chosen = (unsigned char *)malloc((size_t)(L > 0 ? L : 1));
+    for (int b = 0; b < B; ++b) {
+        int n = ctx_lens ? ctx_lens[b] : L;
+        if (n < 0 || n > L) {
+            status = ORACLE_BAD_INPUT;
+            n = n < 0 ? 0 : L;
+        }
+        int32_t *out = idx + (int64_t)b * budget;
+        if (budget >= n) { /* the whole context fits: verify in full */
+            for (int j = 0; j < budget; ++j) out[j] = j < n ? j : -1;
+            if (count) count[b] = n;
+            continue;
+        }
+        const float *ds = draft_score + (int64_t)b * ld;
+        const float *ts = target_score + (int64_t)b * ld;
+        memset(chosen, 0, (size_t)n);
+        int s0 = sink < n ? sink : n;
+        int w0 = window < n - s0 ? window : n - s0;
+        for (int t = 0; t < s0; ++t) chosen[t] = 1;         /* attention sink */
+        for (int t = n - w0; t < n; ++t) chosen[t] = 1;     /* local window   */
+        int rest_lo = s0, rest_hi = n - w0, nrest = rest_hi - rest_lo;
+        int left = budget - s0 - w0;
+        /* tier 1: top-m of the remaining tokens by draft-lookahead score */
+        int m = top_m;
+        if (m > left) m = left;
+        if (m > nrest) m = nrest;
+        for (int t = rest_lo; t < rest_hi; ++t) {
+            pool[t - rest_lo].score = ds[t];
+            pool[t - rest_lo].index = t;
+        }
+        qsort(pool, (size_t)nrest, sizeof(scored_token), cmp_rank);
+        for (int j = 0; j < m; ++j) chosen[pool[j].index] = 1;
+        left -= m;
+        /* tier 2: fill the rest of the budget by target-historical score */
+        int np = 0;
+        for (int t = rest_lo; t < rest_hi; ++t) {
+            if (chosen[t]) continue;
+            pool[np].score = ts[t];
+            pool[np].index = t;
+            ++np;
+        }
+        qsort(pool, (size_t)np, sizeof(scored_token), cmp_rank);
+        for (int j = 0; j < left && j < np; ++j) chosen[pool[j].index] = 1;
+        /* emit ascending */
+        int c = 0;
+        for (int t = 0; t < n; ++t)
+            if (chosen[t]) out[c++] = t;
+        for (int j = c; j < budget; ++j) out[j] = -1;
+        if (count) count[b] = c;
+    }
+    free(pool);
+    free(chosen);
+    return status;
+}
+
+/* ------------------------------------------------------------------------ */
+/* attention                                                                 */
+
+int oracle_attend(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                  int64_t stride_b, int64_t stride_h, int64_t stride_t,
+                  const uint16_t *k_draft, const uint16_t *v_draft, const int32_t *parent,
+                  const int32_t *idx, int budget, int B, int N, int Hq, int Hkv, int d, int L,
+                  const int32_t *ctx_lens, float scale, int64_t cache_begin, int64_t cache_end,
+                  const int64_t *rows, int64_t n_rows, double *out, double *lse)
+{
+    if (B < 1 || N < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || d < 1 || L < 0 || !q || !out ||
+        !lse || !rows || (L > 0 && (!k_cache || !v_cache)) || (idx && budget < 0) ||
+        ((k_draft == NULL) != (v_draft == NULL)) || (k_draft && !parent))
+        return ORACLE_INVALID_ARG;
+    const int G = Hq / Hkv;
+    const double sc = (double)scale;
+    int status = ORACLE_OK;
+
+#pragma omp parallel for schedule(dynamic, 1) reduction(max : status)
+    for (int64_t r = 0; r < n_rows; ++r) {
+        int64_t row = rows[r];
+        int h = (int)(row % Hq);
+        int i = (int)((row / Hq) % N);
+        int b = (int)(row / ((int64_t)Hq * N));
+        int hk = h / G;
+        int n = ctx_lens ? ctx_lens[b] : L;
+        if (n < 0 || n > L) {
+            status = ORACLE_BAD_INPUT;
+            n = n < 0 ? 0 : L;
+        }
+        const uint16_t *qrow = q + (((int64_t)b * N + i) * Hq + h) * d;
+
+        /* cache keys that are candidates at all, in order */
+        int64_t ncache_cand = idx ? budget : n;
+        int64_t nkeys = ncache_cand + N;
+        unsigned char *visible = (unsigned char *)calloc((size_t)(nkeys > 0 ? nkeys : 1), 1);
+        int64_t *token = (int64_t *)malloc(sizeof(int64_t) * (size_t)(ncache_cand > 0 ? ncache_cand : 1));
+        double *s = (double *)malloc(sizeof(double) * (size_t)(nkeys > 0 ? nkeys : 1));
+
+        /* explicit mask, cache part */
+        for (int64_t j = 0; j < ncache_cand; ++j) {
+            int64_t t;
+            if (idx) {
+                const int32_t *ib = idx + (int64_t)b * budget;
+                t = ib[j];
+                int ok = t >= 0 && t < n && (j == 0 || t > ib[j - 1]);
+                if (!ok) {
+                    if (t != -1) status = ORACLE_BAD_INPUT;
+                    continue;
+                }
+            } else {
+                t = j;
+            }
+            if (t < cache_begin || t >= cache_end) continue;
+            token[j] = t;
+            visible[j] = 1;
+        }
+        /* explicit mask, draft part: node i sees itself and its ancestors */
+        if (k_draft) {
+            const int32_t *pb = parent + (int64_t)b * N;
+            visible[ncache_cand + i] = 1;
+            int j = i;
+            while (1) {
+                int p = pb[j];
+                if (p == -1) break;
+                if (p < -1 || p >= j) {
+                    status = ORACLE_BAD_INPUT;
+                    break;
+                }
+                visible[ncache_cand + p] = 1;
+                j = p;
+            }
+        }
+
+        /* scores over all visible keys */
+        double mx = -INFINITY;
+        for (int64_t j = 0; j < nkeys; ++j) {
+            if (!visible[j]) continue;
+            const uint16_t *krow;
+            if (j < ncache_cand)
+                krow = k_cache + b * stride_b + hk * stride_h + token[j] * stride_t;
+            else
+                krow = k_draft + (((int64_t)b * N + (j - ncache_cand)) * Hkv + hk) * d;
+            double dot = 0.0;
+            for (int c = 0; c < d; ++c) dot += bf16_to_double(qrow[c]) * bf16_to_double(krow[c]);
+            s[j] = sc * dot;
+            if (s[j] > mx) mx = s[j];
+        }
+        double *o = out + r * d;
+        for (int c = 0; c < d; ++c) o[c] = 0.0;
+        if (mx == -INFINITY) { /* nothing visible */
+            lse[r] = -INFINITY;
+        } else {
+            double sum = 0.0;
+            for (int64_t j = 0; j < nkeys; ++j)
+                if (visible[j]) sum += exp(s[j] - mx);
+            double l = mx + log(sum);
+            lse[r] = l;
+            for (int64_t j = 0; j < nkeys; ++j) {
+                if (!visible[j]) continue;
+                const uint16_t *vrow;
+                if (j < ncache_cand)
+                    vrow = v_cache + b * stride_b + hk * stride_h + token[j] * stride_t;
+                else
+                    vrow = v_draft + (((int64_t)b * N + (j - ncache_cand)) * Hkv + hk) * d;
+                double p = exp(s[j] - l);
+                for (int c = 0; c < d; ++c) o[c] += p * bf16_to_double(vrow[c]);
+            }
+        }
+        free(visible);
+        free(token);
+        free(s);
+    }
+    return status;
+}
+
+/* ------------------------------------------------------------------------ */
+/* log-sum-exp merge of two normalised parts                                 */
+
+int oracle_lse_merge(const float *o_a, const float *lse_a, const float *o_b, const float *lse_b,
+                     int64_t rows, int d, double *out, double *lse_out)
+{
+    if (rows < 0 || d < 1 || !o_a || !lse_a || !o_b || !lse_b || !out || !lse_out)
+        return ORACLE_INVALID_ARG;
+    for (int64_t r = 0; r < rows; ++r) {
+        double la = lse_a[r], lb = lse_b[r];
+        double m = la > lb ? la : lb;
+        if (isnan(la) || isnan(lb)) m = NAN;
+        double *o = out + r * d;
+        if (m == -INFINITY) { /* neither part saw a key */
+            lse_out[r] = -INFINITY;
+            for (int c = 0; c < d; ++c) o[c] = 0.0;
+            continue;
+        }
+        double l = m + log(exp(la - m) + exp(lb - m));
+        double wa = exp(la - l), wb = exp(lb - l);
+        lse_out[r] = l;
+        for (int c = 0; c < d; ++c) o[c] = wa * (double)o_a[r * d + c] + wb * (double)o_b[r * d + c];
+    }
+    return ORACLE_OK;
+}
