@@ -1,0 +1,186 @@
+/*
+ * specverify.h - C ABI of libspecverify.so: target-model verification attention
+ * for long-context speculative decoding, on one GB300 (sm_103a).
+ *
+ * The operations (source pages, by title and section):
+ *   - "Riepilogo Tecnico: Dustin", Metodologia section 1 (Aggregazione Ibrida
+ *     dell'Attenzione): the verification set I_verify of fixed size = an
+ *     attention-sink prefix + a window of recent tokens + the top-m tokens by
+ *     the draft-lookahead score + a fill by the target-historical score.
+ *   - Dustin, Metodologia section 3 (Workflow di Verifica), steps 3-4: the
+ *     target verifies the draft tokens against the cache restricted to the
+ *     selected tokens; the full cache stays in memory (nothing is evicted).
+ *   - "LongSpec", section 2.C (Hybrid Tree Attention): attention is split into
+ *     the cache part (no mask) and the speculative part (tree mask), and the
+ *     two are combined exactly with the log-sum-exp trick.
+ *
+ * Conventions shared by every entry point:
+ *   - bf16 tensors are passed as `const uint16_t*` holding bf16 bit patterns.
+ *   - Every tensor pointer is a DEVICE pointer on the calling thread's current
+ *     CUDA device, except where a comment says "host".
+ *   - Ownership: the caller owns every buffer; the library allocates nothing
+ *     and keeps no state between calls, apart from the two measurement aids at
+ *     the end of this file (per calling thread).
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and is asynchronous. Results are valid once the stream reaches
+ *     the point after the call.
+ *   - Host-side checks return synchronously, before anything is enqueued:
+ *     SPEC_ERR_INVALID_ARG for null/misaligned pointers or impossible sizes,
+ *     SPEC_ERR_UNSUPPORTED for head_dim != 128 or a device that is not
+ *     compute capability 10.3, SPEC_ERR_WORKSPACE for a workspace that is
+ *     too small. A failed launch returns SPEC_ERR_CUDA.
+ *   - Data-dependent errors found on the device (a parent outside [-1, i), an
+ *     index that is out of range or not strictly ascending, a context length
+ *     outside [0, L]) never trap: the offending entry is treated as masked,
+ *     the rest of the result is computed, and SPEC_ERR_BAD_INPUT is recorded
+ *     in the workspace's status word. Read it with spec_read_device_status().
+ *     Each call clears the status word of its workspace first.
+ *   - Layouts (row-major, innermost last):
+ *       q        [B, N, Hq, d]           bf16   (query of draft node i, head h)
+ *       k_cache, v_cache [B, Hkv, L, d]  bf16   element (b,h,t,c) at
+ *                b*kv_stride_b + h*kv_stride_h + t*kv_stride_t + c
+ *                (strides in elements, multiples of 8; d contiguous)
+ *       k_draft, v_draft [B, N, Hkv, d]  bf16   (this step's draft tokens)
+ *       parent   [B, N] int32: parent[b,i] in [-1, i); -1 = child of the last
+ *                cache token. Node i sees draft node j iff j == i or j is an
+ *                ancestor of i.
+ *       out      [B, N, Hq, d] fp32, lse [B, N, Hq] fp32 (natural log of the
+ *                sum of exp(scale * q.k) over every key the row sees).
+ *     Query head h reads KV head h / (Hq / Hkv) (grouped-query attention).
+ *   - A row that sees no key at all gets out = 0 and lse = -inf.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SPEC_OK = 0,
+    SPEC_ERR_INVALID_ARG = 1,
+    SPEC_ERR_UNSUPPORTED = 2,
+    SPEC_ERR_CUDA = 3,
+    SPEC_ERR_WORKSPACE = 4,
+    SPEC_ERR_BAD_INPUT = 5,
+    SPEC_ERR_TIMEOUT = 6
+} spec_status_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *spec_status_string(int status);
+
+/* ------------------------------------------------------------------------ */
+/* Hybrid top-k selection of I_verify (Dustin, Metodologia section 1).
+ *
+ * For each sequence b with n = ctx_lens[b] (or L when ctx_lens is NULL):
+ *   if budget >= n: idx[b] = 0, 1, ..., n-1, then -1 padding (full context);
+ *   else, with S' = min(sink, n), W' = min(window, n - S'):
+ *     C = [0, S') u [n - W', n)                   (sink and local window)
+ *     R = the other tokens
+ *     D = the min(top_m, budget - |C|, |R|) best of R by draft_score
+ *     F = the budget - |C| - |D| best of R \ D by target_score
+ *     idx[b] = C u D u F in ascending order (exactly `budget` entries).
+ *   "Best" = larger score; -0 == +0; NaN ranks below every number; ties go
+ *   to the lower index. The result is therefore unique (bit-exact).
+ *
+ * draft_score, target_score: fp32 [B, ld] device, row b at b*ld, L <= ld.
+ * ctx_lens: int32 [B] device, or NULL.
+ * idx: int32 [B, budget] device (output). count: int32 [B] device (output:
+ *   number of valid entries, min(budget, n)) or NULL.
+ * Requires 1 <= budget, 0 <= sink, window, top_m, sink + window <= budget,
+ * 1 <= L <= 1572864.
+ * workspace: device, >= spec_select_workspace_size() bytes, 256-byte aligned.
+ */
+size_t spec_select_workspace_size(int B, int L, int budget);
+spec_status_t spec_select_topk(const float *draft_score, const float *target_score, int64_t ld,
+                               int B, int L, const int32_t *ctx_lens, int sink, int window,
+                               int top_m, int budget, int32_t *idx, int32_t *count,
+                               void *workspace, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* Dense verification attention (full cache + tree-masked draft block).
+ *
+ * out[b,i,h] = softmax over { cache tokens 0..n-1 } u { draft nodes visible
+ * to i } of scale * q.k, applied to the matching V rows, where
+ * n = ctx_lens[b] (or L). The cache part is a split-KV pass over the whole
+ * GPU; the partial results and the tree part are merged by log-sum-exp
+ * (LongSpec section 2.C).
+ *
+ * If k_draft == NULL (then v_draft and parent must be NULL too), the tree part
+ * is skipped: the result is the cache-only part, ready to be combined with
+ * another part through spec_lse_merge.
+ * Requires d == 128, Hq % Hkv == 0, 1 <= N <= 4096, B >= 1, L >= 0,
+ * 16-byte aligned tensors; out/lse must not overlap the inputs.
+ * workspace: device, >= spec_verify_workspace_size(B, N, Hq, Hkv, d, L)
+ * bytes, 256-byte aligned; holds the split partials and the status word.
+ */
+size_t spec_verify_workspace_size(int B, int N, int Hq, int Hkv, int d, int L_or_budget);
+spec_status_t spec_verify_attn(const uint16_t *q, const uint16_t *k_cache,
+                               const uint16_t *v_cache, int64_t kv_stride_b,
+                               int64_t kv_stride_h, int64_t kv_stride_t,
+                               const uint16_t *k_draft, const uint16_t *v_draft,
+                               const int32_t *parent, int B, int N, int Hq, int Hkv, int d, int L,
+                               const int32_t *ctx_lens, float scale, float *out, float *lse,
+                               void *workspace, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* Sparse verification attention (Dustin, Workflow di Verifica steps 3-4).
+ *
+ * Same as spec_verify_attn, but the cache part only reads the rows
+ * idx[b, 0..budget) (shared by all heads of sequence b). Entry j is used iff
+ * 0 <= idx[b,j] < n and (j == 0 or idx[b,j] > idx[b,j-1]); -1 entries are
+ * padding and are skipped silently; any other unused entry also records
+ * SPEC_ERR_BAD_INPUT. The workspace size is
+ * spec_verify_workspace_size(B, N, Hq, Hkv, d, budget). The cache rows of
+ * every (b, h) must lie on a common grid of d-element rows: kv_stride_b,
+ * kv_stride_h and kv_stride_t multiples of d.
+ */
+spec_status_t spec_verify_attn_sparse(const uint16_t *q, const uint16_t *k_cache,
+                                      const uint16_t *v_cache, int64_t kv_stride_b,
+                                      int64_t kv_stride_h, int64_t kv_stride_t,
+                                      const uint16_t *k_draft, const uint16_t *v_draft,
+                                      const int32_t *parent, int B, int N, int Hq, int Hkv, int d,
+                                      int L, const int32_t *ctx_lens, float scale,
+                                      const int32_t *idx, int budget, float *out, float *lse,
+                                      void *workspace, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* Log-sum-exp merge of two normalised attention parts (LongSpec section 2.C):
+ *   lse = log(exp(lse_a) + exp(lse_b)),
+ *   out = exp(lse_a - lse) * o_a + exp(lse_b - lse) * o_b,
+ * per row; two parts that both have lse = -inf give out = 0, lse = -inf.
+ * o_a, o_b, out: fp32 [rows, d]; lse_a, lse_b, lse_out: fp32 [rows]; device.
+ * out may alias o_a or o_b, lse_out may alias lse_a or lse_b (in place).
+ */
+spec_status_t spec_lse_merge(const float *o_a, const float *lse_a, const float *o_b,
+                             const float *lse_b, float *out, float *lse_out, int64_t rows, int d,
+                             void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* Synchronises `stream`, then returns the status word that the last call
+ * using `workspace` left there: SPEC_OK or SPEC_ERR_BAD_INPUT (or
+ * SPEC_ERR_TIMEOUT from a bounded wait that gave up). */
+spec_status_t spec_read_device_status(const void *workspace, void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* Measurement aids (per calling thread; not needed for normal use).
+ *
+ * spec_profile_events(start, stop): when both are non-NULL cudaEvent_t
+ * handles, each following spec_verify_attn / spec_verify_attn_sparse call
+ * records `start` on its stream right before its cache-attention kernel and
+ * `stop` right after it, so that the caller can time that kernel alone with
+ * cudaEventElapsedTime. Pass NULL, NULL to stop.
+ *
+ * spec_kernel_launches(): number of CUDA kernels this thread has launched
+ * through the library so far (memsets are not counted). */
+void spec_profile_events(void *start_event, void *stop_event);
+uint64_t spec_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

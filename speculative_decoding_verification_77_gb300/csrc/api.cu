@@ -1,0 +1,235 @@
+// C ABI of libspecverify.so: argument checks, workspace carve-up, dispatch.
+// Every declaration and its contract is in include/specverify.h.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace specverify {
+
+namespace {
+
+thread_local uint64_t g_launches = 0;
+thread_local cudaEvent_t g_prof_start = nullptr;
+thread_local cudaEvent_t g_prof_stop = nullptr;
+
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+    int ok;   // -1 unknown, 0 unsupported, 1 compute capability 10.3
+    int sms;  // multiprocessor count
+};
+DeviceInfo g_dev[kMaxDevices];
+std::once_flag g_dev_once[kMaxDevices];
+
+// Current device's properties (cached per device). Returns SPEC_OK on a cc 10.3 device.
+spec_status_t current_device(DeviceInfo *out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return SPEC_ERR_UNSUPPORTED;
+    }
+    std::call_once(g_dev_once[dev], [dev] {
+        int major = 0, minor = 0, sms = 0;
+        bool good = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+                    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+                    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess;
+        cudaGetLastError();
+        g_dev[dev].ok = good && major == 10 && minor == 3 ? 1 : 0;
+        g_dev[dev].sms = sms > 0 ? sms : 0;
+    });
+    *out = g_dev[dev];
+    return out->ok == 1 ? SPEC_OK : SPEC_ERR_UNSUPPORTED;
+}
+
+// SM count used for sizing: the current device's, else 160 (an upper bound for GB300 parts).
+int sizing_sms() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0)
+        return sms;
+    cudaGetLastError();
+    return 160;
+}
+
+inline bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+constexpr int kMmaCtasPerSm = 2;
+
+SplitPlan verify_plan(int B, int N, int Hq, int Hkv, int L_eff, int sms) {
+    return make_plan(B, N, Hq, Hkv, L_eff, mma_rows_per_unit(), mma_tile_tokens(), sms * kMmaCtasPerSm);
+}
+
+spec_status_t verify_common(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                            int64_t sb, int64_t sh, int64_t st, const uint16_t *k_draft,
+                            const uint16_t *v_draft, const int32_t *parent, int B, int N, int Hq,
+                            int Hkv, int d, int L, const int32_t *ctx_lens, float scale,
+                            const int32_t *idx, int budget, bool sparse, float *out, float *lse,
+                            void *workspace, size_t ws_bytes, void *stream) {
+    // host checks, before anything is enqueued
+    if (!q || !out || !lse || !workspace) return SPEC_ERR_INVALID_ARG;
+    if (B < 1 || N < 1 || N > 4096 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || L < 0) return SPEC_ERR_INVALID_ARG;
+    if (L > 0 && (!k_cache || !v_cache)) return SPEC_ERR_INVALID_ARG;
+    if ((k_draft == nullptr) != (v_draft == nullptr)) return SPEC_ERR_INVALID_ARG;
+    if (k_draft && !parent) return SPEC_ERR_INVALID_ARG;
+    if (sparse && (!idx || budget < 1)) return SPEC_ERR_INVALID_ARG;
+    if (sb < 0 || sh < 0 || st < 0 || sb % 8 || sh % 8 || st % 8) return SPEC_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k_draft, 16) ||
+        !aligned(v_draft, 16) || !aligned(out, 16) || !aligned(lse, 4) || !aligned(workspace, 256) ||
+        !aligned(parent, 4) || !aligned(idx, 4) || !aligned(ctx_lens, 4))
+        return SPEC_ERR_INVALID_ARG;
+    if (!(scale == scale)) return SPEC_ERR_INVALID_ARG;
+    if (d != kHeadDim) return SPEC_ERR_UNSUPPORTED;
+    if (sparse && (sb % d || sh % d || st % d)) return SPEC_ERR_INVALID_ARG;
+    if ((int64_t)B * N * Hq > (int64_t)1 << 31) return SPEC_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (spec_status_t s = current_device(&dev)) return s;
+
+    const SplitPlan plan = verify_plan(B, N, Hq, Hkv, sparse ? budget : L, dev.sms);
+    if (ws_bytes < plan_workspace_bytes(plan, d)) return SPEC_ERR_WORKSPACE;
+
+    VerifyArgs a;
+    a.q = reinterpret_cast<const __nv_bfloat16 *>(q);
+    a.k_cache = reinterpret_cast<const __nv_bfloat16 *>(k_cache);
+    a.v_cache = reinterpret_cast<const __nv_bfloat16 *>(v_cache);
+    a.sb = sb; a.sh = sh; a.st = st;
+    a.k_draft = reinterpret_cast<const __nv_bfloat16 *>(k_draft);
+    a.v_draft = reinterpret_cast<const __nv_bfloat16 *>(v_draft);
+    a.parent = parent;
+    a.ctx_lens = ctx_lens;
+    a.idx = sparse ? idx : nullptr;
+    a.budget = sparse ? budget : 0;
+    a.B = B; a.N = N; a.Hq = Hq; a.Hkv = Hkv; a.G = Hq / Hkv; a.L = L;
+    a.scale = scale;
+    a.out = out;
+    a.lse = lse;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    a.status = reinterpret_cast<uint32_t *>(ws);
+    a.o_part = reinterpret_cast<float *>(ws + kHeaderBytes);
+    a.lse_part = reinterpret_cast<float *>(ws + kHeaderBytes +
+                                           align_up((size_t)plan.slots * plan.BM * d * sizeof(float), 256));
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s) != cudaSuccess) return SPEC_ERR_CUDA;
+    const bool prof = g_prof_start && g_prof_stop;
+    if (launch_cache_attn_mma(a, plan, sparse, s, prof ? g_prof_start : nullptr,
+                              prof ? g_prof_stop : nullptr) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    if (launch_merge_tree(a, plan, s) != cudaSuccess) return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
+}  // namespace
+
+void count_launches(int n) { g_launches += (uint64_t)n; }
+
+}  // namespace specverify
+
+using namespace specverify;
+
+extern "C" {
+
+const char *spec_status_string(int status) {
+    switch (status) {
+        case SPEC_OK: return "SPEC_OK";
+        case SPEC_ERR_INVALID_ARG: return "SPEC_ERR_INVALID_ARG";
+        case SPEC_ERR_UNSUPPORTED: return "SPEC_ERR_UNSUPPORTED";
+        case SPEC_ERR_CUDA: return "SPEC_ERR_CUDA";
+        case SPEC_ERR_WORKSPACE: return "SPEC_ERR_WORKSPACE";
+        case SPEC_ERR_BAD_INPUT: return "SPEC_ERR_BAD_INPUT";
+        case SPEC_ERR_TIMEOUT: return "SPEC_ERR_TIMEOUT";
+        default: return "SPEC_ERR_UNKNOWN";
+    }
+}
+
+size_t spec_select_workspace_size(int B, int L, int budget) {
+    (void)B; (void)L; (void)budget;
+    return kHeaderBytes;
+}
+
+spec_status_t spec_select_topk(const float *draft_score, const float *target_score, int64_t ld,
+                               int B, int L, const int32_t *ctx_lens, int sink, int window,
+                               int top_m, int budget, int32_t *idx, int32_t *count,
+                               void *workspace, size_t ws_bytes, void *stream) {
+    if (!draft_score || !target_score || !idx || !workspace) return SPEC_ERR_INVALID_ARG;
+    if (B < 0 || L < 1 || L > 1572864 || ld < L || sink < 0 || window < 0 || top_m < 0 ||
+        budget < 1 || (int64_t)sink + window > budget)
+        return SPEC_ERR_INVALID_ARG;
+    if (!aligned(draft_score, 4) || !aligned(target_score, 4) || !aligned(idx, 4) ||
+        !aligned(count, 4) || !aligned(ctx_lens, 4) || !aligned(workspace, 256))
+        return SPEC_ERR_INVALID_ARG;
+    if (ws_bytes < spec_select_workspace_size(B, L, budget)) return SPEC_ERR_WORKSPACE;
+    DeviceInfo dev;
+    if (spec_status_t s = current_device(&dev)) return s;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t *status = static_cast<uint32_t *>(workspace);
+    if (cudaMemsetAsync(status, 0, sizeof(uint32_t), s) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (launch_select_topk(draft_score, target_score, ld, B, L, ctx_lens, sink, window, top_m, budget,
+                           idx, count, status, s) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
+size_t spec_verify_workspace_size(int B, int N, int Hq, int Hkv, int d, int L_or_budget) {
+    if (B < 1 || N < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || d < 1 || L_or_budget < 0) return 0;
+    const SplitPlan p = verify_plan(B, N, Hq, Hkv, L_or_budget, sizing_sms());
+    return plan_workspace_bytes(p, d);
+}
+
+spec_status_t spec_verify_attn(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                               int64_t kv_stride_b, int64_t kv_stride_h, int64_t kv_stride_t,
+                               const uint16_t *k_draft, const uint16_t *v_draft,
+                               const int32_t *parent, int B, int N, int Hq, int Hkv, int d, int L,
+                               const int32_t *ctx_lens, float scale, float *out, float *lse,
+                               void *workspace, size_t ws_bytes, void *stream) {
+    return verify_common(q, k_cache, v_cache, kv_stride_b, kv_stride_h, kv_stride_t, k_draft, v_draft,
+                         parent, B, N, Hq, Hkv, d, L, ctx_lens, scale, nullptr, 0, false, out, lse,
+                         workspace, ws_bytes, stream);
+}
+
+spec_status_t spec_verify_attn_sparse(const uint16_t *q, const uint16_t *k_cache,
+                                      const uint16_t *v_cache, int64_t kv_stride_b,
+                                      int64_t kv_stride_h, int64_t kv_stride_t,
+                                      const uint16_t *k_draft, const uint16_t *v_draft,
+                                      const int32_t *parent, int B, int N, int Hq, int Hkv, int d,
+                                      int L, const int32_t *ctx_lens, float scale,
+                                      const int32_t *idx, int budget, float *out, float *lse,
+                                      void *workspace, size_t ws_bytes, void *stream) {
+    return verify_common(q, k_cache, v_cache, kv_stride_b, kv_stride_h, kv_stride_t, k_draft, v_draft,
+                         parent, B, N, Hq, Hkv, d, L, ctx_lens, scale, idx, budget, true, out, lse,
+                         workspace, ws_bytes, stream);
+}
+
+spec_status_t spec_lse_merge(const float *o_a, const float *lse_a, const float *o_b,
+                             const float *lse_b, float *out, float *lse_out, int64_t rows, int d,
+                             void *stream) {
+    if (!o_a || !lse_a || !o_b || !lse_b || !out || !lse_out || rows < 0 || d < 1)
+        return SPEC_ERR_INVALID_ARG;
+    if (!aligned(o_a, 4) || !aligned(o_b, 4) || !aligned(out, 4) || !aligned(lse_a, 4) ||
+        !aligned(lse_b, 4) || !aligned(lse_out, 4))
+        return SPEC_ERR_INVALID_ARG;
+    if (rows > ((int64_t)1 << 36)) return SPEC_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (spec_status_t s = current_device(&dev)) return s;
+    if (launch_lse_merge2(o_a, lse_a, o_b, lse_b, out, lse_out, rows, d,
+                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
+spec_status_t spec_read_device_status(const void *workspace, void *stream) {
+    if (!workspace) return SPEC_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t v = 0;
+    if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SPEC_ERR_CUDA;
+    return static_cast<spec_status_t>(v);
+}
+
+void spec_profile_events(void *start_event, void *stop_event) {
+    g_prof_start = static_cast<cudaEvent_t>(start_event);
+    g_prof_stop = static_cast<cudaEvent_t>(stop_event);
+}
+
+uint64_t spec_kernel_launches(void) { return g_launches; }
+
+}  // extern "C"

@@ -1,0 +1,123 @@
+// Internal helpers shared by the CUDA translation units of libspecverify.so.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/specverify.h"
+
+namespace specverify {
+
+constexpr int kHeadDim = 128;
+constexpr size_t kHeaderBytes = 256;  // status word + reserved, at the start of every workspace
+
+// Status word handling (device side). Never traps: the most severe code wins.
+__device__ __forceinline__ void flag_status(uint32_t *status, uint32_t code) {
+    if (status) atomicMax(status, code);
+}
+
+// ---------------------------------------------------------------------------
+// Split-KV work plan.
+//
+// The cache part is cut into "units" (b, h_kv, row group) of up to BM query
+// rows each, every unit into tiles of `tile` KV positions. The units' tiles
+// are laid end to end (unit-major) and cut into `ctas` contiguous, balanced
+// ranges, one per CTA, so every SM gets the same number of tiles whatever B,
+// Hkv and L are. CTA c covers global tiles [start(c), start(c+1)); for each
+// unit u its range touches, it writes one normalised partial (o, lse) into
+// slot c + u. Along the range both c and u only grow, so c + u is unique per
+// (c, u) pair and the slots number ctas + units - 1.
+struct SplitPlan {
+    int BM;             // query rows per unit (rows of one CTA's tile)
+    int tile;           // KV positions per tile
+    int row_groups;     // ceil(G*N / BM)
+    int units;          // B * Hkv * row_groups
+    int tiles_per_unit; // ceil(L_eff / tile), at least 1
+    int ctas;           // CTAs of the cache kernel
+    int64_t total;      // units * tiles_per_unit
+    int64_t slots;      // ctas + units - 1
+};
+
+__host__ __device__ __forceinline__ int64_t plan_start(const SplitPlan &p, int64_t c) {
+    return c * p.total / p.ctas;
+}
+__host__ __device__ __forceinline__ int64_t plan_cta_of(const SplitPlan &p, int64_t g) {
+    return ((g + 1) * (int64_t)p.ctas - 1) / p.total;
+}
+
+inline SplitPlan make_plan(int B, int N, int Hq, int Hkv, int L_eff, int BM, int tile, int max_ctas) {
+    SplitPlan p;
+    const int G = Hq / Hkv;
+    p.BM = BM;
+    p.tile = tile;
+    p.row_groups = (G * N + BM - 1) / BM;
+    p.units = B * Hkv * p.row_groups;
+    p.tiles_per_unit = L_eff > 0 ? (L_eff + tile - 1) / tile : 1;
+    p.total = (int64_t)p.units * p.tiles_per_unit;
+    p.ctas = (int)(p.total < max_ctas ? p.total : max_ctas);
+    if (p.ctas < 1) p.ctas = 1;
+    p.slots = (int64_t)p.ctas + p.units - 1;
+    return p;
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Workspace carve-up for the verify calls: header | o partials | lse partials.
+inline size_t plan_workspace_bytes(const SplitPlan &p, int d) {
+    size_t o = align_up((size_t)p.slots * p.BM * d * sizeof(float), 256);
+    size_t l = align_up((size_t)p.slots * p.BM * sizeof(float), 256);
+    return kHeaderBytes + o + l;
+}
+
+struct VerifyArgs {
+    const __nv_bfloat16 *q;
+    const __nv_bfloat16 *k_cache;
+    const __nv_bfloat16 *v_cache;
+    int64_t sb, sh, st;  // cache strides in elements
+    const __nv_bfloat16 *k_draft;
+    const __nv_bfloat16 *v_draft;
+    const int32_t *parent;
+    const int32_t *ctx_lens;
+    const int32_t *idx;  // sparse only
+    int budget;          // sparse only
+    int B, N, Hq, Hkv, G, L;
+    float scale;
+    float *out;
+    float *lse;
+    uint32_t *status;
+    float *o_part;    // [slots][BM][d]
+    float *lse_part;  // [slots][BM]
+};
+
+// Context length of sequence b, clamped to [0, L]; out-of-range values flag bad input.
+__device__ __forceinline__ int context_len(const VerifyArgs &a, int b) {
+    if (!a.ctx_lens) return a.L;
+    int n = __ldg(a.ctx_lens + b);
+    if (n < 0 || n > a.L) {
+        flag_status(a.status, SPEC_ERR_BAD_INPUT);
+        n = n < 0 ? 0 : a.L;
+    }
+    return n;
+}
+
+// Tiling of the mma.sync cache kernel (query rows per unit, tokens per tile).
+int mma_rows_per_unit();
+int mma_tile_tokens();
+
+// Host-side launchers (one per translation unit).
+cudaError_t launch_cache_attn_mma(const VerifyArgs &a, const SplitPlan &p, bool sparse,
+                                  cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1);
+cudaError_t launch_merge_tree(const VerifyArgs &a, const SplitPlan &p, cudaStream_t s);
+cudaError_t launch_lse_merge2(const float *o_a, const float *lse_a, const float *o_b,
+                              const float *lse_b, float *out, float *lse_out, int64_t rows, int d,
+                              cudaStream_t s);
+cudaError_t launch_select_topk(const float *ds, const float *ts, int64_t ld, int B, int L,
+                               const int32_t *ctx_lens, int sink, int window, int top_m,
+                               int budget, int32_t *idx, int32_t *count, uint32_t *status,
+                               cudaStream_t s);
+
+// Kernel-launch counter (per host thread), see spec_kernel_launches().
+void count_launches(int n);
+
+}  // namespace specverify

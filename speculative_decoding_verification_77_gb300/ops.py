@@ -1,0 +1,236 @@
+"""Thin PyTorch binding of libspecverify.so (argument marshalling only).
+
+Every step of the computation runs in the library's CUDA kernels; this module
+only checks tensor dtypes/devices, allocates outputs and workspaces with
+torch, and passes raw pointers and the current CUDA stream through ctypes.
+It has no fallback: if the library is missing or the device is not sm_103a,
+the call raises.
+
+Names mirror the C ABI (include/specverify.h):
+  select_topk            -> spec_select_topk
+  verify_attn            -> spec_verify_attn
+  verify_attn_sparse     -> spec_verify_attn_sparse
+  lse_merge              -> spec_lse_merge
+  read_device_status     -> spec_read_device_status
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libspecverify.so")
+
+SPEC_OK = 0
+SPEC_ERR_BAD_INPUT = 5
+STATUS_NAMES = {0: "SPEC_OK", 1: "SPEC_ERR_INVALID_ARG", 2: "SPEC_ERR_UNSUPPORTED", 3: "SPEC_ERR_CUDA",
+                4: "SPEC_ERR_WORKSPACE", 5: "SPEC_ERR_BAD_INPUT", 6: "SPEC_ERR_TIMEOUT"}
+
+# (name, restype, argtypes) of every exported entry point
+P, I, I64, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "spec_status_string": (ctypes.c_char_p, [I]),
+    "spec_select_workspace_size": (SZ, [I, I, I]),
+    "spec_select_topk": (I, [P, P, I64, I, I, P, I, I, I, I, P, P, P, SZ, P]),
+    "spec_verify_workspace_size": (SZ, [I, I, I, I, I, I]),
+    "spec_verify_attn": (I, [P, P, P, I64, I64, I64, P, P, P, I, I, I, I, I, I, P, F, P, P, P, SZ, P]),
+    "spec_verify_attn_sparse": (I, [P, P, P, I64, I64, I64, P, P, P, I, I, I, I, I, I, P, F, P, I,
+                                    P, P, P, SZ, P]),
+    "spec_lse_merge": (I, [P, P, P, P, P, P, I64, I, P]),
+    "spec_read_device_status": (I, [P, P]),
+    "spec_profile_events": (None, [P, P]),
+    "spec_kernel_launches": (ctypes.c_uint64, []),
+}
+
+_lib = None
+
+
+class SpecError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(code, code)}")
+        self.code = code
+
+
+def load_library(path: str = LIB_PATH):
+    """Load the C-ABI library (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"libspecverify.so not built ({path}); run __graft_entry__.build()")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _check(fn: str, code: int):
+    if code != SPEC_OK:
+        raise SpecError(fn, code)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(t: torch.Tensor):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _need(t, dtype, name, dims=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if dims is not None and t.dim() != dims:
+        raise ValueError(f"{name} must have {dims} dims, got {tuple(t.shape)}")
+
+
+_workspaces: dict = {}
+
+
+def workspace(nbytes: int, device: torch.device, key: str = "default") -> torch.Tensor:
+    """A cached uint8 device buffer of at least nbytes (one per device, stream and key)."""
+    stream = torch.cuda.current_stream(device).cuda_stream
+    k = (device.index, stream, key)
+    ws = _workspaces.get(k)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _workspaces[k] = ws
+    return ws
+
+
+def select_topk(draft_score: torch.Tensor, target_score: torch.Tensor, *, sink: int, window: int,
+                top_m: int, budget: int, ctx_lens: torch.Tensor | None = None,
+                idx: torch.Tensor | None = None, count: torch.Tensor | None = None,
+                ws: torch.Tensor | None = None):
+    """Hybrid sink/window/top-m/fill selection. Scores fp32 [B, L] (row stride = stride(0))."""
+    lib = load_library()
+    _need(draft_score, torch.float32, "draft_score", 2)
+    _need(target_score, torch.float32, "target_score", 2)
+    _need(ctx_lens, torch.int32, "ctx_lens", 1)
+    if draft_score.stride(1) != 1 or target_score.stride(1) != 1 or \
+            draft_score.stride(0) != target_score.stride(0):
+        raise ValueError("score rows must be contiguous with a common row stride")
+    B, L = draft_score.shape
+    dev = draft_score.device
+    if idx is None:
+        idx = torch.empty((B, budget), dtype=torch.int32, device=dev)
+    if count is None:
+        count = torch.empty((B,), dtype=torch.int32, device=dev)
+    nbytes = lib.spec_select_workspace_size(B, L, budget)
+    if ws is None:
+        ws = workspace(nbytes, dev, "select")
+    _check("spec_select_topk", lib.spec_select_topk(
+        _ptr(draft_score), _ptr(target_score), draft_score.stride(0), B, L, _ptr(ctx_lens), sink, window,
+        top_m, budget, _ptr(idx), _ptr(count), _ptr(ws), ws.numel(), _stream(draft_score)))
+    return idx, count
+
+
+def _verify(q, k_cache, v_cache, k_draft, v_draft, parent, scale, ctx_lens, idx, out, lse, ws):
+    lib = load_library()
+    _need(q, torch.bfloat16, "q", 4)
+    _need(k_cache, torch.bfloat16, "k_cache", 4)
+    _need(v_cache, torch.bfloat16, "v_cache", 4)
+    _need(k_draft, torch.bfloat16, "k_draft", 4)
+    _need(v_draft, torch.bfloat16, "v_draft", 4)
+    _need(parent, torch.int32, "parent", 2)
+    _need(ctx_lens, torch.int32, "ctx_lens", 1)
+    _need(idx, torch.int32, "idx", 2)
+    B, N, Hq, d = q.shape
+    _, Hkv, L, _ = k_cache.shape
+    if not q.is_contiguous():
+        raise ValueError("q must be contiguous [B, N, Hq, d]")
+    if k_cache.stride() != v_cache.stride() or k_cache.shape != v_cache.shape or k_cache.stride(3) != 1:
+        raise ValueError("k_cache and v_cache must share shape and strides, with d contiguous")
+    for t, nm in ((k_draft, "k_draft"), (v_draft, "v_draft")):
+        if t is not None and (not t.is_contiguous() or tuple(t.shape) != (B, N, Hkv, d)):
+            raise ValueError(f"{nm} must be contiguous [B, N, Hkv, d]")
+    if parent is not None and (not parent.is_contiguous() or tuple(parent.shape) != (B, N)):
+        raise ValueError("parent must be contiguous int32 [B, N]")
+    if idx is not None and (not idx.is_contiguous() or idx.shape[0] != B):
+        raise ValueError("idx must be contiguous int32 [B, budget]")
+    if scale is None:
+        scale = d ** -0.5
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, N, Hq, d), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((B, N, Hq), dtype=torch.float32, device=dev)
+    L_eff = idx.shape[1] if idx is not None else L
+    nbytes = lib.spec_verify_workspace_size(B, N, Hq, Hkv, d, L_eff)
+    if ws is None:
+        ws = workspace(nbytes, dev, "verify")
+    sb, sh, st = k_cache.stride(0), k_cache.stride(1), k_cache.stride(2)
+    common = (_ptr(q), _ptr(k_cache), _ptr(v_cache), sb, sh, st, _ptr(k_draft), _ptr(v_draft),
+              _ptr(parent), B, N, Hq, Hkv, d, L, _ptr(ctx_lens), ctypes.c_float(scale))
+    if idx is None:
+        code = lib.spec_verify_attn(*common, _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(q))
+        _check("spec_verify_attn", code)
+    else:
+        code = lib.spec_verify_attn_sparse(*common, _ptr(idx), idx.shape[1], _ptr(out), _ptr(lse),
+                                           _ptr(ws), ws.numel(), _stream(q))
+        _check("spec_verify_attn_sparse", code)
+    return out, lse
+
+
+def verify_attn(q, k_cache, v_cache, k_draft=None, v_draft=None, parent=None, *, scale=None,
+                ctx_lens=None, out=None, lse=None, ws=None):
+    """Dense verification attention: full cache + tree-masked draft block, LSE-merged.
+
+    q [B,N,Hq,d] bf16; k_cache/v_cache [B,Hkv,L,d] bf16 (any strides with d contiguous);
+    k_draft/v_draft [B,N,Hkv,d] bf16 and parent int32 [B,N], or all None (cache-only part).
+    Returns (out fp32 [B,N,Hq,d], lse fp32 [B,N,Hq]).
+    """
+    return _verify(q, k_cache, v_cache, k_draft, v_draft, parent, scale, ctx_lens, None, out, lse, ws)
+
+
+def verify_attn_sparse(q, k_cache, v_cache, k_draft, v_draft, parent, idx, *, scale=None,
+                       ctx_lens=None, out=None, lse=None, ws=None):
+    """Sparse verification attention over the cache rows idx[b] (int32 [B, budget])."""
+    return _verify(q, k_cache, v_cache, k_draft, v_draft, parent, scale, ctx_lens, idx, out, lse, ws)
+
+
+def lse_merge(o_a, lse_a, o_b, lse_b, out=None, lse_out=None):
+    """Merge two normalised parts by log-sum-exp. o [..., d] fp32, lse [...] fp32."""
+    lib = load_library()
+    for t, nm in ((o_a, "o_a"), (lse_a, "lse_a"), (o_b, "o_b"), (lse_b, "lse_b")):
+        _need(t, torch.float32, nm)
+        if not t.is_contiguous():
+            raise ValueError(f"{nm} must be contiguous")
+    d = o_a.shape[-1]
+    rows = lse_a.numel()
+    if o_a.numel() != rows * d or o_b.numel() != rows * d or lse_b.numel() != rows:
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty_like(o_a)
+    if lse_out is None:
+        lse_out = torch.empty_like(lse_a)
+    _check("spec_lse_merge", lib.spec_lse_merge(_ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), _ptr(out),
+                                                _ptr(lse_out), rows, d, _stream(o_a)))
+    return out, lse_out
+
+
+def read_device_status(ws: torch.Tensor) -> int:
+    """Synchronise the current stream and read the status word the last call left in ws."""
+    return load_library().spec_read_device_status(_ptr(ws), _stream(ws))
+
+
+def kernel_launches() -> int:
+    return load_library().spec_kernel_launches()
+
+
+def profile_events(start: torch.cuda.Event | None, stop: torch.cuda.Event | None):
+    """Record start/stop around the cache-attention kernel of following verify calls (None: off)."""
+    lib = load_library()
+    if start is None or stop is None:
+        lib.spec_profile_events(None, None)
+    else:
+        lib.spec_profile_events(ctypes.c_void_p(start.cuda_event), ctypes.c_void_p(stop.cuda_event))

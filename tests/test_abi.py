@@ -1,0 +1,118 @@
+"""C-ABI checks that need no GPU: the library loads, exports every declared
+symbol, and rejects bad arguments on the host before touching CUDA."""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "specverify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_verification_77_gb300 import build, ops
+
+    build.build()
+    return ops.load_library()
+
+
+def declared_functions():
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for must in ("spec_select_topk", "spec_verify_attn", "spec_verify_attn_sparse", "spec_lse_merge",
+                 "spec_select_workspace_size", "spec_verify_workspace_size", "spec_read_device_status"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from speculative_decoding_verification_77_gb300 import ops
+
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in ops.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    assert lib.spec_status_string(0) == b"SPEC_OK"
+    assert lib.spec_status_string(5) == b"SPEC_ERR_BAD_INPUT"
+    assert lib.spec_status_string(99) == b"SPEC_ERR_UNKNOWN"
+
+
+def test_workspace_sizes(lib):
+    a = lib.spec_verify_workspace_size(4, 64, 32, 8, 128, 32768)
+    b = lib.spec_verify_workspace_size(8, 64, 32, 8, 128, 32768)
+    assert 256 < a < b
+    assert lib.spec_verify_workspace_size(1, 1, 3, 2, 128, 10) == 0  # Hq % Hkv != 0
+    assert lib.spec_select_workspace_size(16, 32768, 2048) >= 4
+
+
+def _verify_args(**over):
+    F = ctypes.c_float
+    args = dict(q=16, kc=16, vc=16, sb=0, sh=0, st=128, kd=None, vd=None, par=None, B=1, N=1, Hq=1, Hkv=1,
+                d=128, L=4, ctx=None, scale=F(0.1), out=16, lse=16, ws=256, ws_bytes=1 << 30, stream=None)
+    args.update(over)
+    return list(args.values())
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), 1),                      # null pointer
+    (dict(N=0), 1),                         # no draft node
+    (dict(Hq=3, Hkv=2), 1),                 # Hq % Hkv != 0
+    (dict(q=24), 1),                        # misaligned
+    (dict(kd=16, vd=None), 1),              # draft K without V
+    (dict(kd=16, vd=16, par=None), 1),      # draft block without parents
+    (dict(st=100), 1),                      # stride not a multiple of 8
+    (dict(ws=128), 1),                      # workspace not 256-aligned
+    (dict(d=64), 2),                        # head_dim other than 128
+])
+def test_verify_rejects_bad_arguments_on_the_host(lib, over, code):
+    # fake, never-dereferenced addresses: the checks return before any CUDA call
+    assert lib.spec_verify_attn(*_verify_args(**over)) == code
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(budget=0), 1), (dict(sink=3, window=3, budget=5), 1), (dict(L=0), 1),
+    (dict(ld=10, L=20), 1), (dict(top_m=-1), 1), (dict(idx=None), 1), (dict(L=2_000_000, ld=2_000_000), 1),
+])
+def test_select_rejects_bad_arguments_on_the_host(lib, over, code):
+    a = dict(ds=16, ts=16, ld=100, B=1, L=100, ctx=None, sink=1, window=1, top_m=2, budget=10, idx=16,
+             count=None, ws=256, ws_bytes=256, stream=None)
+    a.update(over)
+    assert lib.spec_select_topk(*a.values()) == code
+
+
+def test_merge_rejects_bad_arguments_on_the_host(lib):
+    assert lib.spec_lse_merge(None, 4, 4, 4, 4, 4, 10, 128, None) == 1
+    assert lib.spec_lse_merge(4, 4, 4, 4, 4, 4, -1, 128, None) == 1
+    assert lib.spec_lse_merge(4, 4, 4, 4, 4, 4, 10, 0, None) == 1
+
+
+def test_package_import_loads_nothing():
+    import importlib
+    import sys
+
+    mod = importlib.import_module("speculative_decoding_verification_77_gb300")
+    assert "speculative_decoding_verification_77_gb300.ops" not in sys.modules or mod is not None
+
+
+def test_product_does_not_use_the_oracle():
+    """The product package must neither import nor call the oracle."""
+    pkg = os.path.join(ROOT, "speculative_decoding_verification_77_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".cpp", ".h")):
+                with open(os.path.join(dirpath, fn)) as f:
+                    src = f.read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", src, re.M), fn
+                assert "spec_oracle" not in src and "oracle_attend" not in src, fn

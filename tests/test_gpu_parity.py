@@ -1,0 +1,339 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Tolerances (from the arithmetic the path must meet): selection indices
+bit-exact; attention outputs within max-abs 1e-2 of the fp64 oracle and,
+because |o| is only ~0.01 for flat softmax at long context, also within
+2e-2 * max|o_ref| (relative infinity norm); lse within 1e-3 absolute.
+Large workloads are checked on sampled rows, which the oracle computes one by
+one; needles at tile and split boundaries catch a skipped or doubled tile that
+the flat-softmax tolerance could miss.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_verification_77_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+ATOL_O, RTOL_O, ATOL_L = 1e-2, 2e-2, 1e-3
+
+
+@pytest.fixture(scope="module")
+def ops():
+    from speculative_decoding_verification_77_gb300 import ops as o
+
+    o.load_library()
+    return o
+
+
+def dev():
+    return torch.device("cuda:0")
+
+
+def to_dev(x):
+    return {k: (v.to(dev()) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+
+
+def assert_attn_close(out, lse, ro, rl, rows=None):
+    o = out.float().cpu().numpy().reshape(-1, out.shape[-1])
+    l_ = lse.float().cpu().numpy().reshape(-1)
+    if rows is not None:
+        o, l_ = o[rows], l_[rows]
+    assert np.all(np.isfinite(o)), "non-finite output"
+    err = np.abs(o - ro).max()
+    ref = np.abs(ro).max()
+    assert err <= ATOL_O, f"max-abs {err}"
+    assert err <= RTOL_O * ref + 1e-7, f"relative {err / ref}"
+    fin = np.isfinite(rl)
+    assert np.array_equal(np.isfinite(l_), fin)
+    assert np.abs(l_[fin] - rl[fin]).max(initial=0) <= ATOL_L, f"lse {np.abs(l_[fin] - rl[fin]).max()}"
+
+
+def sample_rows(B, N, Hq, k, seed=0):
+    rng = np.random.default_rng(seed)
+    total = B * N * Hq
+    rows = set(rng.choice(total, size=min(k, total), replace=False).tolist())
+    rows |= {0, total - 1, Hq - 1, (N - 1) * Hq}
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def run_dense(ops, x, g, rows=None, **kw):
+    out, lse = ops.verify_attn(g["q"], g["k_cache"], g["v_cache"], g["k_draft"], g["v_draft"], g["parent"],
+                               scale=x["scale"], ctx_lens=kw.get("ctx_lens_dev"))
+    ro, rl, st = oracle.attend(x["q"], x["k_cache"], x["v_cache"], x["k_draft"], x["v_draft"], x["parent"],
+                               scale=x["scale"], rows=rows, ctx_lens=kw.get("ctx_lens"))
+    assert st == 0
+    torch.cuda.synchronize()
+    assert_attn_close(out, lse, ro, rl, rows)
+    return out, lse
+
+
+# ---------------------------------------------------------------------------
+# the five workloads
+
+
+def test_workload1_tiny_dense_all_rows(ops):
+    x = W.make_inputs(W.workload(1))
+    run_dense(ops, x, to_dev(x))
+
+
+def test_workload2_llama_layer_sampled(ops):
+    x = W.make_inputs(W.workload(2))
+    w = x["workload"]
+    run_dense(ops, x, to_dev(x), rows=sample_rows(w.B, w.N, w.Hq, 384))
+
+
+def test_workload3_sparse_hybrid(ops):
+    w = W.workload(3)
+    x = W.make_inputs(w)
+    g = to_dev(x)
+    idx, cnt = ops.select_topk(g["draft_score"], g["target_score"], sink=w.sink, window=w.window,
+                               top_m=w.top_m, budget=w.budget)
+    ridx, rcnt, st = oracle.select(x["draft_score"], x["target_score"], sink=w.sink, window=w.window,
+                                   top_m=w.top_m, budget=w.budget)
+    assert st == 0
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    assert np.array_equal(cnt.cpu().numpy(), rcnt)
+    out, lse = ops.verify_attn_sparse(g["q"], g["k_cache"], g["v_cache"], g["k_draft"], g["v_draft"],
+                                      g["parent"], idx, scale=x["scale"])
+    rows = sample_rows(w.B, w.N, w.Hq, 512)
+    ro, rl, st = oracle.attend(x["q"], x["k_cache"], x["v_cache"], x["k_draft"], x["v_draft"], x["parent"],
+                               scale=x["scale"], idx=torch.from_numpy(ridx), rows=rows)
+    assert st == 0
+    assert_attn_close(out, lse, ro, rl, rows)
+
+
+def test_workload4_qwen_layer_sampled(ops):
+    x = W.make_inputs(W.workload(4))
+    w = x["workload"]
+    run_dense(ops, x, to_dev(x), rows=sample_rows(w.B, w.N, w.Hq, 96))
+
+
+@pytest.mark.parametrize("N", [1, 4, 16, 64, 256])
+def test_workload5_tree_sweep_sampled(ops, N):
+    x = W.make_inputs(W.workload(5, N))
+    w = x["workload"]
+    run_dense(ops, x, to_dev(x), rows=sample_rows(w.B, w.N, w.Hq, 160, seed=N))
+
+
+# ---------------------------------------------------------------------------
+# edge cases
+
+
+def small(seed, B=2, N=5, Hq=8, Hkv=2, L=333, tree="random", depth=3):
+    w = W.Workload("edge", B=B, L=L, Hq=Hq, Hkv=Hkv, N=N, tree=tree, depth_max=depth, seed=seed)
+    return W.make_inputs(w)
+
+
+@pytest.mark.parametrize("L", [0, 1, 63, 64, 65, 200, 1000])
+def test_ragged_lengths_and_tails(ops, L):
+    x = small(L + 1, L=L)
+    run_dense(ops, x, to_dev(x))
+
+
+def test_ragged_ctx_lens(ops):
+    x = small(3, B=4, L=777)
+    cl = torch.tensor([777, 700, 5, 0], dtype=torch.int32)
+    run_dense(ops, x, to_dev(x), ctx_lens=cl, ctx_lens_dev=cl.to(dev()))
+
+
+@pytest.mark.parametrize("tree", ["chain", "star", "forest"])
+def test_tree_shapes(ops, tree):
+    x = small(11, N=12, L=300, tree="chain")
+    if tree == "star":
+        x["parent"] = torch.full((2, 12), -1, dtype=torch.int32)
+    elif tree == "forest":
+        x["parent"] = torch.tensor([[-1, 0, -1, 2, 1, -1, 5, 6, 3, 8, -1, 10]] * 2, dtype=torch.int32)
+    run_dense(ops, x, to_dev(x))
+
+
+@pytest.mark.parametrize("N,Hq,Hkv", [(300, 4, 1), (17, 16, 2), (1, 1, 1), (33, 12, 4)])
+def test_row_groups_and_head_ratios(ops, N, Hq, Hkv):
+    x = small(5, B=1, N=N, Hq=Hq, Hkv=Hkv, L=500, depth=6)
+    run_dense(ops, x, to_dev(x))
+
+
+def test_cache_only_then_merge_equals_full(ops):
+    x = small(21, L=900)
+    g = to_dev(x)
+    full_o, full_l = ops.verify_attn(g["q"], g["k_cache"], g["v_cache"], g["k_draft"], g["v_draft"],
+                                     g["parent"], scale=x["scale"])
+    co, cl = ops.verify_attn(g["q"], g["k_cache"], g["v_cache"], scale=x["scale"])
+    # tree part alone: an empty cache
+    e = g["k_cache"][:, :, :0]
+    to, tl = ops.verify_attn(g["q"], e, e, g["k_draft"], g["v_draft"], g["parent"], scale=x["scale"])
+    mo, ml = ops.lse_merge(co, cl, to, tl)
+    torch.cuda.synchronize()
+    assert torch.allclose(mo, full_o, atol=1e-5, rtol=0)
+    assert torch.allclose(ml, full_l, atol=1e-5, rtol=0)
+    # each part against the oracle, and the merge against the oracle's merge
+    ro, rl, _ = oracle.attend(x["q"], x["k_cache"], x["v_cache"], None, None, x["parent"], scale=x["scale"])
+    assert_attn_close(co, cl, ro, rl)
+    mo_ref, ml_ref = oracle.lse_merge(co.cpu(), cl.cpu(), to.cpu(), tl.cpu())
+    np.testing.assert_allclose(mo.cpu().numpy().reshape(mo_ref.shape), mo_ref, atol=1e-6, rtol=0)
+    np.testing.assert_allclose(ml.cpu().numpy().reshape(-1), ml_ref, atol=1e-5, rtol=0)
+
+
+def test_lse_merge_special_rows_and_in_place(ops):
+    rows, d = 1000, 128
+    gen = torch.Generator().manual_seed(3)
+    oa = torch.randn(rows, d, generator=gen)
+    ob = torch.randn(rows, d, generator=gen)
+    la = torch.randn(rows, generator=gen) * 5
+    lb = torch.randn(rows, generator=gen) * 5
+    la[:10] = -math.inf
+    lb[5:15] = -math.inf
+    oa[:10] = 0
+    ob[5:15] = 0
+    ref_o, ref_l = oracle.lse_merge(oa, la, ob, lb)
+    go, gl = oa.to(dev()), la.to(dev())
+    ops.lse_merge(go, gl, ob.to(dev()), lb.to(dev()), out=go, lse_out=gl)  # in place
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(go.cpu().numpy(), ref_o, atol=1e-5, rtol=0)
+    got_l = gl.cpu().numpy()
+    assert np.array_equal(np.isinf(got_l), np.isinf(ref_l))
+    fin = np.isfinite(ref_l)
+    np.testing.assert_allclose(got_l[fin], ref_l[fin], atol=1e-5, rtol=0)
+
+
+@pytest.mark.parametrize("pos", [0, 63, 64, 127, 128, 4095, 4096, 9999])
+def test_needle_positions(ops, pos):
+    """One key with logit ~ +30 at tile/split boundaries: o must be that key's V."""
+    x = small(pos, B=1, N=2, Hq=4, Hkv=2, L=10000)
+    q = x["q"]
+    scale = x["scale"]
+    qv = q[0, 0, 2].double()
+    x["k_cache"][0, 1, pos] = (qv * (30.0 / (scale * float(qv.dot(qv))))).to(torch.bfloat16)
+    rows = np.array([2])
+    g = to_dev(x)
+    out, lse = ops.verify_attn(g["q"], g["k_cache"], g["v_cache"], g["k_draft"], g["v_draft"], g["parent"],
+                               scale=scale)
+    ro, rl, _ = oracle.attend(x["q"], x["k_cache"], x["v_cache"], x["k_draft"], x["v_draft"], x["parent"],
+                              scale=scale, rows=rows)
+    torch.cuda.synchronize()
+    o = out.cpu().numpy().reshape(-1, 128)[2]
+    assert np.abs(o - x["v_cache"][0, 1, pos].float().numpy()).max() < 2e-2
+    assert_attn_close(out, lse, ro, rl, rows)
+
+
+def test_strided_cache_layout(ops):
+    """K/V as [B, L, Hkv, d] memory viewed as [B, Hkv, L, d] (token-major cache)."""
+    x = small(8, B=2, L=400, Hq=8, Hkv=4)
+    kc = x["k_cache"].permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3)
+    g = to_dev(x)
+    gk = x["k_cache"].permute(0, 2, 1, 3).contiguous().to(dev()).permute(0, 2, 1, 3)
+    gv = x["v_cache"].permute(0, 2, 1, 3).contiguous().to(dev()).permute(0, 2, 1, 3)
+    assert gk.stride() == kc.stride()
+    out, lse = ops.verify_attn(g["q"], gk, gv, g["k_draft"], g["v_draft"], g["parent"], scale=x["scale"])
+    ro, rl, _ = oracle.attend(x["q"], x["k_cache"], x["v_cache"], x["k_draft"], x["v_draft"], x["parent"],
+                              scale=x["scale"])
+    torch.cuda.synchronize()
+    assert_attn_close(out, lse, ro, rl)
+
+
+def test_sparse_budget_covering_context_equals_dense(ops):
+    x = small(31, L=500)
+    g = to_dev(x)
+    idx = torch.cat([torch.arange(500, dtype=torch.int32), torch.full((12,), -1, dtype=torch.int32)])
+    idx = idx.repeat(2, 1).to(dev())
+    so, sl = ops.verify_attn_sparse(g["q"], g["k_cache"], g["v_cache"], g["k_draft"], g["v_draft"],
+                                    g["parent"], idx, scale=x["scale"])
+    do, dl = ops.verify_attn(g["q"], g["k_cache"], g["v_cache"], g["k_draft"], g["v_draft"], g["parent"],
+                             scale=x["scale"])
+    torch.cuda.synchronize()
+    assert torch.allclose(so, do, atol=1e-5, rtol=0) and torch.allclose(sl, dl, atol=1e-5, rtol=0)
+
+
+def test_sparse_ragged_selection(ops):
+    x = small(41, B=3, L=2000, N=6)
+    ds, ts = W.random_scores(3, 2000, seed=4, ties=6)
+    cl = torch.tensor([2000, 1500, 100], dtype=torch.int32)
+    g = to_dev(x)
+    kw = dict(sink=4, window=64, top_m=128, budget=300)
+    idx, cnt = ops.select_topk(ds.to(dev()), ts.to(dev()), ctx_lens=cl.to(dev()), **kw)
+    ridx, rcnt, _ = oracle.select(ds, ts, ctx_lens=cl, **kw)
+    assert np.array_equal(idx.cpu().numpy(), ridx) and np.array_equal(cnt.cpu().numpy(), rcnt)
+    out, lse = ops.verify_attn_sparse(g["q"], g["k_cache"], g["v_cache"], g["k_draft"], g["v_draft"],
+                                      g["parent"], idx, scale=x["scale"], ctx_lens=cl.to(dev()))
+    ro, rl, _ = oracle.attend(x["q"], x["k_cache"], x["v_cache"], x["k_draft"], x["v_draft"], x["parent"],
+                              scale=x["scale"], idx=torch.from_numpy(ridx), ctx_lens=cl)
+    torch.cuda.synchronize()
+    assert_attn_close(out, lse, ro, rl)
+
+
+@pytest.mark.parametrize("case", ["ties", "special", "small_ctx", "big_top_m", "zero_top_m"])
+def test_selection_cases_bit_exact(ops, case):
+    B, L = 5, 5000
+    ds, ts = W.random_scores(B, L, seed=7, ties=3 if case == "ties" else 0)
+    kw = dict(sink=4, window=64, top_m=512, budget=1024)
+    cl = None
+    if case == "special":
+        rng = np.random.default_rng(0)
+        for arr in (ds, ts):
+            pick = rng.choice(B * L, size=2000, replace=False)
+            vals = np.array([np.nan, -0.0, 0.0, np.inf, -np.inf], np.float32)
+            arr.view(-1)[torch.from_numpy(pick)] = torch.from_numpy(rng.choice(vals, size=2000))
+    if case == "small_ctx":
+        cl = torch.tensor([5000, 1024, 1025, 68, 0], dtype=torch.int32)
+    if case == "big_top_m":
+        kw["top_m"] = 5000
+    if case == "zero_top_m":
+        kw["top_m"] = 0
+    idx, cnt = ops.select_topk(ds.to(dev()), ts.to(dev()), ctx_lens=None if cl is None else cl.to(dev()), **kw)
+    ridx, rcnt, _ = oracle.select(ds, ts, ctx_lens=cl, **kw)
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    assert np.array_equal(cnt.cpu().numpy(), rcnt)
+
+
+def test_bad_inputs_set_the_status_word(ops):
+    x = small(51, L=300, tree="chain")
+    g = to_dev(x)
+    ws = torch.zeros(1 << 24, dtype=torch.uint8, device=dev())
+    ops.verify_attn(g["q"], g["k_cache"], g["v_cache"], g["k_draft"], g["v_draft"], g["parent"],
+                    scale=x["scale"], ws=ws)
+    assert ops.read_device_status(ws) == 0
+    bad = g["parent"].clone()
+    bad[0, 3] = 7  # parent after the node
+    out, lse = ops.verify_attn(g["q"], g["k_cache"], g["v_cache"], g["k_draft"], g["v_draft"], bad,
+                               scale=x["scale"], ws=ws)
+    assert ops.read_device_status(ws) == 5
+    ro, rl, st = oracle.attend(x["q"], x["k_cache"], x["v_cache"], x["k_draft"], x["v_draft"], bad.cpu(),
+                               scale=x["scale"])
+    assert st == 5
+    assert_attn_close(out, lse, ro, rl)
+    idx = torch.tensor([[0, 5, 5, 2, 999, -1], [1, 2, 3, -1, -1, -1]], dtype=torch.int32)
+    out, lse = ops.verify_attn_sparse(g["q"], g["k_cache"], g["v_cache"], g["k_draft"], g["v_draft"],
+                                      g["parent"], idx.to(dev()), scale=x["scale"], ws=ws)
+    assert ops.read_device_status(ws) == 5
+    ro, rl, _ = oracle.attend(x["q"], x["k_cache"], x["v_cache"], x["k_draft"], x["v_draft"], x["parent"],
+                              scale=x["scale"], idx=idx)
+    assert_attn_close(out, lse, ro, rl)
+    # a clean call clears the word again
+    ops.verify_attn(g["q"], g["k_cache"], g["v_cache"], g["k_draft"], g["v_draft"], g["parent"],
+                    scale=x["scale"], ws=ws)
+    assert ops.read_device_status(ws) == 0
+
+
+def test_native_kernels_ran(ops):
+    before = ops.kernel_launches()
+    x = small(61, L=100)
+    g = to_dev(x)
+    ops.verify_attn(g["q"], g["k_cache"], g["v_cache"], g["k_draft"], g["v_draft"], g["parent"])
+    torch.cuda.synchronize()
+    assert ops.kernel_launches() >= before + 2
+
+
+def test_workspace_too_small_is_rejected(ops):
+    x = small(71, L=100)
+    g = to_dev(x)
+    ws = torch.zeros(512, dtype=torch.uint8, device=dev())
+    with pytest.raises(ops.SpecError) as e:
+        ops.verify_attn(g["q"], g["k_cache"], g["v_cache"], g["k_draft"], g["v_draft"], g["parent"], ws=ws)
+    assert e.value.code == 4
