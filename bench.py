@@ -138,7 +138,7 @@ def oracle_baseline(x, rows_target_s: float = 10.0, max_rows: int | None = None)
     elapsed = 0.0
     done = 0
     while True:
-        rows = rng.choice(total_rows, size=min(n, total_rows), replace=False)
+        rows = rng.choice(total_rows, size=min(n, total_rows - done), replace=False)
         t = time.perf_counter()
         oracle.attend(x["q"], x["k_cache"], x["v_cache"], x["k_draft"], x["v_draft"], x["parent"],
                       scale=x["scale"], rows=rows)
