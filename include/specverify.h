@@ -160,6 +160,42 @@ spec_status_t spec_lse_merge(const float *o_a, const float *lse_a, const float *
                              void *stream);
 
 /* ------------------------------------------------------------------------ */
+/* Dense verification attention without a workspace (allocates nothing).
+ *
+ * The source pages have no counterpart to this entry point: it is a
+ * deployment convenience. Some callers cannot allocate device memory at call
+ * time - serving engines that reserve almost all of HBM for the KV cache at
+ * start-up and allow no later allocation, or hosts that reach this library
+ * from a plain C callback with no allocator - so they cannot pass the
+ * workspace spec_verify_attn needs. This variant computes the same result with
+ * the same kernels, but keeps its scratch (split partials and status word) in
+ * a fixed 16 MiB array inside the library (every GPU that loads the library
+ * holds it until the process exits). It calls no cudaMalloc, cudaFree or
+ * other allocating routine.
+ *
+ * Arguments are those of spec_verify_attn without the workspace, plus
+ * status_out: int32 device pointer that receives SPEC_OK or
+ * SPEC_ERR_BAD_INPUT for this call's data, or NULL.
+ * Limits: the problem's split partials must fit the built-in scratch; larger
+ * problems return SPEC_ERR_WORKSPACE (use spec_verify_attn). For example
+ * B=4, L=32768, Hq=32, Hkv=8, N=64 fits on a 152-SM GB300; B=8, Hq=64,
+ * Hkv=8, N=32 does not.
+ * The first call on each device looks up the array's device address (once,
+ * with that device current); make that first call before any stream capture.
+ * Every call on a device shares the one array: calls that overlap on the GPU
+ * (different streams or threads, not ordered by the caller) race with each
+ * other and must not be issued.
+ */
+spec_status_t spec_verify_attn_noalloc(const uint16_t *q, const uint16_t *k_cache,
+                                       const uint16_t *v_cache, int64_t kv_stride_b,
+                                       int64_t kv_stride_h, int64_t kv_stride_t,
+                                       const uint16_t *k_draft, const uint16_t *v_draft,
+                                       const int32_t *parent, int B, int N, int Hq, int Hkv,
+                                       int d, int L, const int32_t *ctx_lens, float scale,
+                                       float *out, float *lse, int32_t *status_out,
+                                       void *stream);
+
+/* ------------------------------------------------------------------------ */
 /* Synchronises `stream`, then returns the status word that the last call
  * using `workspace` left there: SPEC_OK or SPEC_ERR_BAD_INPUT (or
  * SPEC_ERR_TIMEOUT from a bounded wait that gave up). */

@@ -40,6 +40,7 @@ SIGNATURES = {
     "spec_verify_attn_sparse": (I, [P, P, P, I64, I64, I64, P, P, P, I, I, I, I, I, I, P, F, P, I,
                                     P, P, P, SZ, P]),
     "spec_lse_merge": (I, [P, P, P, P, P, P, I64, I, P]),
+    "spec_verify_attn_noalloc": (I, [P, P, P, I64, I64, I64, P, P, P, I, I, I, I, I, I, P, F, P, P, P, P]),
     "spec_read_device_status": (I, [P, P]),
     "spec_profile_events": (None, [P, P]),
     "spec_kernel_launches": (ctypes.c_uint64, []),
