@@ -58,6 +58,13 @@ SplitPlan verify_plan(int B, int N, int Hq, int Hkv, int L_eff, int sms) {
     return make_plan(B, N, Hq, Hkv, L_eff, mma_rows_per_unit(), mma_tile_tokens(), sms * kMmaCtasPerSm);
 }
 
+// Workspace that covers either cache kernel's plan.
+size_t verify_bytes_any(int B, int N, int Hq, int Hkv, int d, int L_eff, int sms) {
+    const size_t a = plan_workspace_bytes(verify_plan(B, N, Hq, Hkv, L_eff, sms), d);
+    const size_t b = plan_workspace_bytes(make_plan_tc(B, N, Hq, Hkv, L_eff, sms), d);
+    return a > b ? a : b;
+}
+
 spec_status_t verify_common(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                             int64_t sb, int64_t sh, int64_t st, const uint16_t *k_draft,
                             const uint16_t *v_draft, const int32_t *parent, int B, int N, int Hq,
@@ -83,8 +90,8 @@ spec_status_t verify_common(const uint16_t *q, const uint16_t *k_cache, const ui
     DeviceInfo dev;
     if (spec_status_t s = current_device(&dev)) return s;
 
-    const SplitPlan plan = verify_plan(B, N, Hq, Hkv, sparse ? budget : L, dev.sms);
-    if (ws_bytes < plan_workspace_bytes(plan, d)) return SPEC_ERR_WORKSPACE;
+    const int L_eff = sparse ? budget : L;
+    if (ws_bytes < verify_bytes_any(B, N, Hq, Hkv, d, L_eff, dev.sms)) return SPEC_ERR_WORKSPACE;
 
     VerifyArgs a;
     a.q = reinterpret_cast<const __nv_bfloat16 *>(q);
@@ -103,16 +110,27 @@ spec_status_t verify_common(const uint16_t *q, const uint16_t *k_cache, const ui
     a.lse = lse;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     a.status = reinterpret_cast<uint32_t *>(ws);
-    a.o_part = reinterpret_cast<float *>(ws + kHeaderBytes);
-    a.lse_part = reinterpret_cast<float *>(ws + kHeaderBytes +
-                                           align_up((size_t)plan.slots * plan.BM * d * sizeof(float), 256));
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s) != cudaSuccess) return SPEC_ERR_CUDA;
-    const bool prof = g_prof_start && g_prof_stop;
-    if (launch_cache_attn_mma(a, plan, sparse, s, prof ? g_prof_start : nullptr,
-                              prof ? g_prof_stop : nullptr) != cudaSuccess)
-        return SPEC_ERR_CUDA;
+    cudaEvent_t ev0 = g_prof_start && g_prof_stop ? g_prof_start : nullptr;
+    cudaEvent_t ev1 = ev0 ? g_prof_stop : nullptr;
+    // dense: the tensor-core (tcgen05/TMA) kernel when the shape allows its TMA maps;
+    // sparse and the other shapes: the warp-level tensor-core kernel
+    SplitPlan plan;
+    bool launched = false;
+    if (!sparse && tc_supported(a)) {
+        plan = make_plan_tc(B, N, Hq, Hkv, L_eff, dev.sms);
+        a.o_part = reinterpret_cast<float *>(ws + kHeaderBytes);
+        a.lse_part = reinterpret_cast<float *>(ws + kHeaderBytes + plan_o_bytes(plan, d));
+        if (launch_cache_attn_tc(a, plan, s, ev0, ev1, &launched) != cudaSuccess) return SPEC_ERR_CUDA;
+    }
+    if (!launched) {
+        plan = verify_plan(B, N, Hq, Hkv, L_eff, dev.sms);
+        a.o_part = reinterpret_cast<float *>(ws + kHeaderBytes);
+        a.lse_part = reinterpret_cast<float *>(ws + kHeaderBytes + plan_o_bytes(plan, d));
+        if (launch_cache_attn_mma(a, plan, sparse, s, ev0, ev1) != cudaSuccess) return SPEC_ERR_CUDA;
+    }
     if (launch_merge_tree(a, plan, s) != cudaSuccess) return SPEC_ERR_CUDA;
     return SPEC_OK;
 }
@@ -170,8 +188,7 @@ spec_status_t spec_select_topk(const float *draft_score, const float *target_sco
 
 size_t spec_verify_workspace_size(int B, int N, int Hq, int Hkv, int d, int L_or_budget) {
     if (B < 1 || N < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || d < 1 || L_or_budget < 0) return 0;
-    const SplitPlan p = verify_plan(B, N, Hq, Hkv, L_or_budget, sizing_sms());
-    return plan_workspace_bytes(p, d);
+    return verify_bytes_any(B, N, Hq, Hkv, d, L_or_budget, sizing_sms());
 }
 
 spec_status_t spec_verify_attn(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,

@@ -1,0 +1,471 @@
+// Cache part of verification attention on the 5th-generation tensor core
+// (tcgen05 + TMEM + TMA), for the dense full-cache case.
+//
+// What it computes is the same normalised split-KV partial as the warp-level
+// kernel: for every unit (b, h_kv, group of query rows: the query heads of
+// h_kv times the draft nodes, packed together) and every range of 128-token
+// KV tiles of the split plan, softmax(scale * Q K^T) V over the cache tokens of
+// that range, with no mask but "token < n" (the cache part needs none, LongSpec
+// section 2.C). Partials are merged by log-sum-exp with the tree part later.
+//
+// Design (one CTA per SM, persistent over its balanced range of tiles):
+//   warp 8      TMA producer: the unit's Q rows (3-D map over [B*N, Hq, d], so
+//               query heads x draft nodes land as consecutive rows), then a
+//               5-slot ring of K and V tiles (4-D map over [B, Hkv, L, d] with
+//               the caller's strides), 128-byte swizzle.
+//   warp 9      MMA issuer (one thread): S_h = Q_h K^T (A and B from shared
+//               memory) and O_h += P_h V (P from TMEM, V MN-major from shared
+//               memory), fp32 accumulators in TMEM, tcgen05.commit to mbarriers.
+//   warps 0-3,  softmax for pipe 0 / pipe 1: thread i owns TMEM lane i = query
+//   warps 4-7   row i; loads its S row, takes the online max in base 2, writes
+//               P = 2^(x - m) as bf16 back over S for the PV MMA. The O
+//               accumulator is only rescaled when the running max grows by more
+//               than 2^8 (exact: l and O always share the same reference max).
+// Two pipes ping-pong on the tensor core. With more than 128 query rows per
+// unit the pipes take rows 0-127 and 128-255 of every tile; with at most 128
+// rows they take alternate tiles of the same rows and each writes its own
+// partial. TMEM (512 columns): S_0, S_1, O_0, O_1, 128 columns each.
+// Every wait on an mbarrier is bounded; a wait that gives up records
+// SPEC_ERR_TIMEOUT, the CTA drains its in-flight copies and MMAs, frees TMEM
+// and returns.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "sm100.cuh"
+
+namespace specverify {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int D = kHeadDim;
+constexpr int T = 128;                // tokens per tile
+constexpr int RING = 5;               // K/V slots
+constexpr int SLOT_BYTES = T * D * 2; // 32 KiB: one K or V tile
+constexpr int HALF_BYTES = SLOT_BYTES / 2;
+constexpr int Q_BYTES = 256 * D * 2;  // 64 KiB
+constexpr int SMEM_RING = Q_BYTES;
+constexpr int SMEM_BAR = SMEM_RING + RING * SLOT_BYTES;  // 229376
+constexpr int SMEM_BYTES = SMEM_BAR + 256 + 1024;        // + barriers + alignment slack
+constexpr int THREADS = 320;
+constexpr int WARP_PRODUCER = 8, WARP_MMA = 9;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, false);
+constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 128, true);
+constexpr long long WAIT_LIMIT_CYCLES = 4000000000LL;  // ~2 s
+
+struct Bars {
+    uint64_t q_full, q_empty;
+    uint64_t kv_full[RING], kv_empty[RING];
+    uint64_t s_full[2], p_full[2], o_done[2], o_empty[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    uint32_t abort;
+};
+
+struct TcParams {
+    int split_tiles;  // 1: pipes take alternate tiles of the same <=128 rows
+    int M;            // G * N query rows per (b, h_kv)
+};
+
+// Bounded wait: false (and the abort flag set) if the phase does not complete in time.
+__device__ __forceinline__ bool wait_bar(Bars &bs, uint64_t *bar, uint32_t parity, uint32_t *status) {
+    if (*(volatile uint32_t *)&bs.abort) return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*(volatile uint32_t *)&bs.abort) return false;
+        if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+            atomicExch(&bs.abort, 1u);
+            flag_status(status, SPEC_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Wait used while draining after an abort: ignores the abort flag, still bounded.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity) && clock64() - t0 < WAIT_LIMIT_CYCLES) {
+    }
+}
+
+// Segment of the CTA's tile range inside one unit.
+struct Seg {
+    int64_t u;
+    int tb, te;  // tiles [tb, te) of the unit
+    int b, hk, rg;
+    int cnt[2];  // tiles per pipe
+};
+
+__device__ __forceinline__ void seg_decode(const VerifyArgs &a, const SplitPlan &p, int split_tiles, int64_t u,
+                                           int64_t g0, int64_t g1, Seg &s) {
+    const int64_t ub = u * p.tiles_per_unit;
+    s.u = u;
+    s.tb = (int)((g0 > ub ? g0 : ub) - ub);
+    s.te = (int)((g1 < ub + p.tiles_per_unit ? g1 : ub + p.tiles_per_unit) - ub);
+    s.rg = (int)(u % p.row_groups);
+    s.hk = (int)((u / p.row_groups) % a.Hkv);
+    s.b = (int)(u / ((int64_t)p.row_groups * a.Hkv));
+    const int nt = s.te - s.tb;
+    s.cnt[0] = split_tiles ? (nt + 1) / 2 : nt;
+    s.cnt[1] = split_tiles ? nt / 2 : nt;
+}
+__device__ __forceinline__ int seg_tile(const Seg &s, int split_tiles, int h, int i) {
+    return split_tiles ? s.tb + 2 * i + h : s.tb + i;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
+                     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    uint8_t *sQ = smem;
+    uint8_t *sRing = smem + SMEM_RING;
+    Bars &bs = *reinterpret_cast<Bars *>(smem + SMEM_BAR);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int split_tiles = tp.split_tiles;
+    const int BM = p.BM;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bs.q_full, 1);
+        mbar_init(&bs.q_empty, 1);
+        for (int i = 0; i < RING; ++i) {
+            mbar_init(&bs.kv_full[i], 1);
+            mbar_init(&bs.kv_empty[i], 1);
+        }
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(&bs.s_full[h], 1);
+            mbar_init(&bs.p_full[h], 4);
+            mbar_init(&bs.o_done[h], 1);
+            mbar_init(&bs.o_empty[h], 4);
+        }
+        mbar_init(&bs.mma_done, 1);
+        bs.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == WARP_PRODUCER) {
+        tmem_alloc(&bs.tmem_base, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bs.tmem_base;
+
+    const int64_t g0 = plan_start(p, blockIdx.x), g1 = plan_start(p, blockIdx.x + 1);
+    const int64_t u_first = g0 / p.tiles_per_unit;
+
+    if (warp == WARP_PRODUCER) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            int64_t item = 0;  // K/V tiles loaded so far (K and V count separately)
+            int seg_i = 0, q_loads = 0;
+            bool ok = true;
+            for (int64_t u = u_first; ok && u * p.tiles_per_unit < g1; ++u, ++seg_i) {
+                Seg s;
+                seg_decode(a, p, split_tiles, u, g0, g1, s);
+                // Q rows of this unit, once the previous unit's QK MMAs are done with them
+                if (seg_i > 0 && !(ok = wait_bar(bs, &bs.q_empty, (seg_i - 1) & 1, a.status))) break;
+                const int npipe_q = split_tiles ? 1 : 2;
+                mbar_arrive_expect_tx(&bs.q_full, npipe_q * 2 * 16384);
+                ++q_loads;
+                for (int h = 0; h < npipe_q; ++h) {
+                    const int n0 = (s.rg * BM + 128 * h) / a.G;
+                    for (int kh = 0; kh < 2; ++kh)
+                        tma_load_3d(sQ + kh * 32768 + h * 16384, &tm_q, &bs.q_full, kh * 64, s.hk * a.G,
+                                    s.b * a.N + n0);
+                }
+                // K and V tiles in order: tile tb: K, V; tile tb+1: K, V; ...
+                for (int t = s.tb; t < s.te; ++t) {
+                    for (int kv = 0; kv < 2; ++kv, ++item) {
+                        const int slot = (int)(item % RING);
+                        const int64_t use = item / RING;
+                        if (use > 0 && !(ok = wait_bar(bs, &bs.kv_empty[slot], (uint32_t)((use - 1) & 1), a.status)))
+                            break;
+                        uint8_t *dst = sRing + slot * SLOT_BYTES;
+                        mbar_arrive_expect_tx(&bs.kv_full[slot], SLOT_BYTES);
+                        const CUtensorMap *m = kv == 0 ? &tm_k : &tm_v;
+                        tma_load_4d(dst, m, &bs.kv_full[slot], 0, t * T, s.hk, s.b);
+                        tma_load_4d(dst + HALF_BYTES, m, &bs.kv_full[slot], 64, t * T, s.hk, s.b);
+                    }
+                    if (!ok) break;
+                }
+            }
+            // drain: wait for the last copies still in flight (consumed ones return at once)
+            const int64_t first = item > RING ? item - RING : 0;
+            for (int64_t n = first; n < item; ++n) drain_wait(&bs.kv_full[n % RING], (uint32_t)((n / RING) & 1));
+            if (q_loads > 0) drain_wait(&bs.q_full, (q_loads - 1) & 1);
+        }
+        __syncwarp();
+    } else if (warp == WARP_MMA) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int64_t item_base = 0;
+            int seg_i = 0;
+            uint32_t pv_count[2] = {0, 0};   // PV MMAs issued per pipe
+            uint32_t pipe_segs[2] = {0, 0};  // segments in which the pipe produced a partial
+            bool ok = true;
+            const uint32_t q_base = smem_u32(sQ), ring_base = smem_u32(sRing);
+            for (int64_t u = u_first; ok && u * p.tiles_per_unit < g1; ++u, ++seg_i) {
+                Seg s;
+                seg_decode(a, p, split_tiles, u, g0, g1, s);
+                if (!(ok = wait_bar(bs, &bs.q_full, seg_i & 1, a.status))) break;
+                tc_fence_after();
+                const int qk_total = s.cnt[0] + s.cnt[1];
+                int qk_done = 0;
+                auto issue_qk = [&](int h, int i) -> bool {
+                    const int t = seg_tile(s, split_tiles, h, i);
+                    const int64_t n = item_base + 2 * (int64_t)(t - s.tb);
+                    const int slot = (int)(n % RING);
+                    if (!wait_bar(bs, &bs.kv_full[slot], (uint32_t)((n / RING) & 1), a.status)) return false;
+                    tc_fence_after();
+                    const uint32_t qa = q_base + (split_tiles ? 0u : (uint32_t)h * 16384u);
+                    const uint32_t kb = ring_base + slot * SLOT_BYTES;
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t off = (uint32_t)(ks >> 2) * 32768u + (uint32_t)(ks & 3) * 32u;
+                        const uint32_t offk = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
+                        mma_ss(tmem + 128u * h, desc_sw128(qa + off, 16, 1024), desc_sw128(kb + offk, 16, 1024),
+                               IDESC_QK, ks > 0);
+                    }
+                    mma_commit(&bs.s_full[h]);
+                    if (split_tiles || h == 1) mma_commit(&bs.kv_empty[slot]);
+                    if (++qk_done == qk_total) mma_commit(&bs.q_empty);
+                    return true;
+                };
+                auto issue_pv = [&](int h, int i) -> bool {
+                    const int t = seg_tile(s, split_tiles, h, i);
+                    if (!wait_bar(bs, &bs.p_full[h], pv_count[h] & 1, a.status)) return false;
+                    if (i == 0 && pipe_segs[h] > 0 &&
+                        !wait_bar(bs, &bs.o_empty[h], (pipe_segs[h] - 1) & 1, a.status))
+                        return false;
+                    const int64_t n = item_base + 2 * (int64_t)(t - s.tb) + 1;
+                    const int slot = (int)(n % RING);
+                    if (!wait_bar(bs, &bs.kv_full[slot], (uint32_t)((n / RING) & 1), a.status)) return false;
+                    tc_fence_after();
+                    const uint32_t vb = ring_base + slot * SLOT_BYTES;
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_ts(tmem + 256u + 128u * h, tmem + 128u * h + 8u * ks,
+                               desc_sw128(vb + 2048u * ks, 16384, 1024), IDESC_PV, (i > 0 || ks > 0));
+                    mma_commit(&bs.o_done[h]);
+                    if (split_tiles || h == 1) mma_commit(&bs.kv_empty[slot]);
+                    ++pv_count[h];
+                    return true;
+                };
+                for (int h = 0; ok && h < 2; ++h)
+                    if (s.cnt[h] > 0) ok = issue_qk(h, 0);
+                const int n_iter = s.cnt[0];
+                for (int i = 0; ok && i < n_iter; ++i)
+                    for (int h = 0; ok && h < 2; ++h) {
+                        if (i >= s.cnt[h]) continue;
+                        ok = issue_pv(h, i);
+                        if (ok && i + 1 < s.cnt[h]) ok = issue_qk(h, i + 1);
+                    }
+                for (int h = 0; h < 2; ++h)
+                    if (s.cnt[h] > 0) ++pipe_segs[h];
+                item_base += 2 * (int64_t)(s.te - s.tb);
+            }
+            // drain: every MMA issued so far must complete before TMEM is freed
+            mma_commit(&bs.mma_done);
+            drain_wait(&bs.mma_done, 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax warps
+        const int h = warp >> 2;            // pipe
+        const int lg = warp & 3;            // TMEM lane group of this warp
+        const int row = lg * 32 + lane;     // row of the pipe = TMEM lane
+        const uint32_t lane_addr = (uint32_t)(lg * 32) << 16;
+        const uint32_t s_col = 128u * h, o_col = 256u + 128u * h;
+        const float sl2 = a.scale * 1.4426950408889634f;  // scores in base 2
+        uint32_t s_count = 0, pv_signaled = 0;
+        bool ok = true;
+        for (int64_t u = u_first; u * p.tiles_per_unit < g1; ++u) {
+            Seg s;
+            seg_decode(a, p, split_tiles, u, g0, g1, s);
+            const int row0 = s.rg * BM + (split_tiles ? 0 : 128 * h);  // first unit row of this pipe
+            const int real_rows = min(max(tp.M - row0, 0), 128);
+            const bool warp_rows = lg * 32 < real_rows;
+            const int64_t slot = (((int64_t)blockIdx.x + u) << 1) + h;
+            float *orow = a.o_part + (slot * 128 + row) * D;
+            float *lrow = a.lse_part + slot * 128 + row;
+            if (s.cnt[h] == 0) {  // this pipe got no tile of the unit: an empty partial
+                if (row < real_rows) {
+                    for (int c = 0; c < D; c += 4) *reinterpret_cast<float4 *>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+                    *lrow = -INFINITY;
+                }
+                continue;
+            }
+            const int n_ctx = context_len(a, s.b);
+            float m_ref = -INFINITY, l = 0.f;
+            for (int k = 0; k < s.cnt[h]; ++k) {
+                const int t = seg_tile(s, split_tiles, h, k);
+                ok = __all_sync(0xffffffffu, ok && wait_bar(bs, &bs.s_full[h], s_count & 1, a.status));
+                ++s_count;
+                tc_fence_after();
+                if (ok && warp_rows) {
+                    uint32_t r[4][32];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_addr + s_col + 32u * c, r[c]);
+                    tmem_wait_ld();
+                    const int valid = min(max(n_ctx - t * T, 0), T);  // tokens of this tile inside the context
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float x = (32 * c + j < valid) ? __uint_as_float(r[c][j]) * sl2 : -INFINITY;
+                            r[c][j] = __float_as_uint(x);
+                            mx = fmaxf(mx, x);
+                        }
+                    // move the reference max only when it grows by more than 2^8
+                    bool rescale_o = false;
+                    float factor = 1.f;
+                    if (mx > m_ref + 8.f) {
+                        factor = ex2(m_ref - mx);  // m_ref = -inf -> 0
+                        rescale_o = l > 0.f;
+                        l *= factor;
+                        m_ref = mx;
+                    }
+                    if (__any_sync(0xffffffffu, rescale_o) && k > 0) {
+                        // O holds the previous tiles: wait for their PV, then rescale this warp's rows
+                        ok = __all_sync(0xffffffffu, ok && wait_bar(bs, &bs.o_done[h], (pv_signaled - 1) & 1, a.status));
+                        tc_fence_after();
+                        if (ok) {
+                            const float f = rescale_o ? factor : 1.f;
+#pragma unroll 1
+                            for (int c = 0; c < 4; ++c) {
+                                uint32_t o[32];
+                                tmem_ld32(tmem + lane_addr + o_col + 32u * c, o);
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
+                                tmem_st32(tmem + lane_addr + o_col + 32u * c, o);
+                            }
+                            tmem_wait_st();
+                        }
+                    }
+                    const float mref = m_ref == -INFINITY ? 0.f : m_ref;
+                    float sum = 0.f;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float p0 = ex2(__uint_as_float(r[c][2 * j]) - mref);
+                            const float p1 = ex2(__uint_as_float(r[c][2 * j + 1]) - mref);
+                            sum += p0 + p1;
+                            __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
+                            pk[j] = *reinterpret_cast<uint32_t *>(&v);
+                        }
+                        tmem_st16(tmem + lane_addr + s_col + 16u * c, pk);
+                    }
+                    l += sum;
+                    tmem_wait_st();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bs.p_full[h]);
+                ++pv_signaled;
+            }
+            // epilogue: O / l and lse of this pipe's rows -> partial slot
+            ok = __all_sync(0xffffffffu, ok && wait_bar(bs, &bs.o_done[h], (pv_signaled - 1) & 1, a.status));
+            tc_fence_after();
+            if (ok && warp_rows) {
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tmem + lane_addr + o_col + 32u * c, o);
+                    tmem_wait_ld();
+                    if (row < real_rows) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<float4 *>(orow + 32 * c + j) =
+                                make_float4(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv,
+                                            __uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
+                    }
+                }
+                if (row < real_rows) *lrow = l > 0.f ? (m_ref + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bs.o_empty[h]);
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == WARP_PRODUCER) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// ---------------------------------------------------------------- host side
+
+bool encode_map(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
+                const cuuint32_t *box) {
+    static const PFN_cuTensorMapEncodeTiled_v12000 encode = [] {
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        const bool found = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                            cudaEnableDefault, &q) == cudaSuccess &&
+                           q == cudaDriverEntryPointSuccess;
+        cudaGetLastError();
+        return found ? reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn) : nullptr;
+    }();
+    if (!encode) return false;
+    cuuint32_t elem[4] = {1, 1, 1, 1};
+    CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), dims,
+                        strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool tc_supported(const VerifyArgs &a) {
+    return a.L >= 1 && a.G >= 1 && a.G <= 128 && (128 % a.G) == 0 && !a.idx;
+}
+
+cudaError_t launch_cache_attn_tc(const VerifyArgs &a, const SplitPlan &p, cudaStream_t s, cudaEvent_t ev0,
+                                 cudaEvent_t ev1, bool *launched) {
+    *launched = false;
+    CUtensorMap mq, mk, mv;
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.Hq, (cuuint64_t)a.B * a.N};
+        const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.Hq * D * 2};
+        const cuuint32_t box[3] = {64, (cuuint32_t)a.G, (cuuint32_t)(128 / a.G)};
+        if (!encode_map(&mq, a.q, 3, dims, strides, box)) return cudaSuccess;
+    }
+    {
+        const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)a.L, (cuuint64_t)a.Hkv, (cuuint64_t)a.B};
+        const cuuint64_t strides[3] = {(cuuint64_t)a.st * 2, (cuuint64_t)a.sh * 2, (cuuint64_t)a.sb * 2};
+        const cuuint32_t box[4] = {64, (cuuint32_t)T, 1, 1};
+        if (!encode_map(&mk, a.k_cache, 4, dims, strides, box)) return cudaSuccess;
+        if (!encode_map(&mv, a.v_cache, 4, dims, strides, box)) return cudaSuccess;
+    }
+    TcParams tp;
+    tp.M = a.G * a.N;
+    tp.split_tiles = tp.M <= 128 ? 1 : 0;
+    cudaError_t e = cudaFuncSetAttribute(cache_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (ev0) cudaEventRecord(ev0, s);
+    cache_attn_tc_kernel<<<p.ctas, THREADS, SMEM_BYTES, s>>>(a, p, tp, mq, mk, mv);
+    e = cudaGetLastError();
+    if (ev1) cudaEventRecord(ev1, s);
+    count_launches(1);
+    *launched = true;
+    return e;
+}
+
+}  // namespace specverify

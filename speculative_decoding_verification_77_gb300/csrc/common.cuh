@@ -36,7 +36,11 @@ struct SplitPlan {
     int tiles_per_unit; // ceil(L_eff / tile), at least 1
     int ctas;           // CTAs of the cache kernel
     int64_t total;      // units * tiles_per_unit
-    int64_t slots;      // ctas + units - 1
+    int64_t slots;      // (ctas + units - 1) * pipes
+    int pipes;          // partial slots per (cta, unit) pair
+    int slot_rows;      // rows per slot
+    int split_tiles;    // 1: the pipes cover alternate tiles of the same rows (both slots per row);
+                        // 0: pipe h covers rows [h*slot_rows, (h+1)*slot_rows) of the unit
 };
 
 __host__ __device__ __forceinline__ int64_t plan_start(const SplitPlan &p, int64_t c) {
@@ -57,17 +61,33 @@ inline SplitPlan make_plan(int B, int N, int Hq, int Hkv, int L_eff, int BM, int
     p.total = (int64_t)p.units * p.tiles_per_unit;
     p.ctas = (int)(p.total < max_ctas ? p.total : max_ctas);
     if (p.ctas < 1) p.ctas = 1;
+    p.pipes = 1;
+    p.slot_rows = BM;
+    p.split_tiles = 0;
     p.slots = (int64_t)p.ctas + p.units - 1;
+    return p;
+}
+
+// Plan of the tensor-core cache kernel: units of 256 query rows (128 when G*N <= 128),
+// 128-token tiles, one CTA per SM, two pipes of 128 rows each writing their own slots.
+inline SplitPlan make_plan_tc(int B, int N, int Hq, int Hkv, int L_eff, int sms) {
+    const int M = (Hq / Hkv) * N;
+    SplitPlan p = make_plan(B, N, Hq, Hkv, L_eff, M > 128 ? 256 : 128, 128, sms);
+    p.pipes = 2;
+    p.slot_rows = 128;
+    p.split_tiles = M <= 128 ? 1 : 0;
+    p.slots = ((int64_t)p.ctas + p.units - 1) * 2;
     return p;
 }
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace carve-up for the verify calls: header | o partials | lse partials.
+inline size_t plan_o_bytes(const SplitPlan &p, int d) {
+    return align_up((size_t)p.slots * p.slot_rows * d * sizeof(float), 256);
+}
 inline size_t plan_workspace_bytes(const SplitPlan &p, int d) {
-    size_t o = align_up((size_t)p.slots * p.BM * d * sizeof(float), 256);
-    size_t l = align_up((size_t)p.slots * p.BM * sizeof(float), 256);
-    return kHeaderBytes + o + l;
+    return kHeaderBytes + plan_o_bytes(p, d) + align_up((size_t)p.slots * p.slot_rows * sizeof(float), 256);
 }
 
 struct VerifyArgs {
@@ -109,6 +129,9 @@ int mma_tile_tokens();
 cudaError_t launch_cache_attn_mma(const VerifyArgs &a, const SplitPlan &p, bool sparse,
                                   cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1);
 cudaError_t launch_merge_tree(const VerifyArgs &a, const SplitPlan &p, cudaStream_t s);
+bool tc_supported(const VerifyArgs &a);
+cudaError_t launch_cache_attn_tc(const VerifyArgs &a, const SplitPlan &p, cudaStream_t s, cudaEvent_t ev0,
+                                 cudaEvent_t ev1, bool *launched);
 cudaError_t launch_lse_merge2(const float *o_a, const float *lse_a, const float *o_b,
                               const float *lse_b, float *out, float *lse_out, int64_t rows, int d,
                               cudaStream_t s);

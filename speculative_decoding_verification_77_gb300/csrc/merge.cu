@@ -53,18 +53,25 @@ __global__ void __launch_bounds__(256) merge_tree_kernel(VerifyArgs a, SplitPlan
     const int b = warp / (a.Hq * a.N);
     const int hk = h / a.G, g = h % a.G;
     const int rfull = i * a.G + g;
-    const int rg = rfull / p.BM, r = rfull % p.BM;
+    const int rg = rfull / p.BM, ru = rfull % p.BM;
     const int64_t u = ((int64_t)b * a.Hkv + hk) * p.row_groups + rg;
+    // which pipe slots hold this row, and the row inside a slot
+    const int h_lo = p.split_tiles ? 0 : ru / p.slot_rows;
+    const int h_hi = p.split_tiles ? p.pipes - 1 : h_lo;
+    const int r = p.split_tiles ? ru : ru % p.slot_rows;
 
     OnlineRow st;
-    // cache part: the normalised partials of every CTA that covered this unit
+    // cache part: the normalised partials of every CTA (and pipe) that covered this unit
     const int64_t c_lo = plan_cta_of(p, u * p.tiles_per_unit);
     const int64_t c_hi = plan_cta_of(p, (u + 1) * p.tiles_per_unit - 1);
     for (int64_t c = c_lo; c <= c_hi; ++c) {
-        const int64_t slot = c + u;
-        const float w = a.lse_part[slot * p.BM + r];
-        const float4 o = *reinterpret_cast<const float4 *>(a.o_part + (slot * p.BM + r) * kHeadDim + 4 * lane);
-        st.add(w, o);
+        for (int hh = h_lo; hh <= h_hi; ++hh) {
+            const int64_t slot = (c + u) * p.pipes + hh;
+            const float w = a.lse_part[slot * p.slot_rows + r];
+            const float4 o =
+                *reinterpret_cast<const float4 *>(a.o_part + (slot * p.slot_rows + r) * kHeadDim + 4 * lane);
+            st.add(w, o);
+        }
     }
     // speculative part: node i and its ancestors (tree mask)
     if (a.k_draft) {

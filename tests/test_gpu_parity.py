@@ -247,8 +247,14 @@ def test_sparse_budget_covering_context_equals_dense(ops):
                                     g["parent"], idx, scale=x["scale"])
     do, dl = ops.verify_attn(g["q"], g["k_cache"], g["v_cache"], g["k_draft"], g["v_draft"], g["parent"],
                              scale=x["scale"])
+    ro, rl, _ = oracle.attend(x["q"], x["k_cache"], x["v_cache"], x["k_draft"], x["v_draft"], x["parent"],
+                              scale=x["scale"])
     torch.cuda.synchronize()
-    assert torch.allclose(so, do, atol=1e-5, rtol=0) and torch.allclose(sl, dl, atol=1e-5, rtol=0)
+    # the sparse and dense paths run different cache kernels: each must meet the oracle,
+    # and they agree with each other to the bf16 rounding of P
+    assert_attn_close(so, sl, ro, rl)
+    assert_attn_close(do, dl, ro, rl)
+    assert torch.allclose(so, do, atol=2e-3, rtol=0) and torch.allclose(sl, dl, atol=1e-4, rtol=0)
 
 
 def test_sparse_ragged_selection(ops):
