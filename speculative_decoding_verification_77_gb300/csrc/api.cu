@@ -91,6 +91,9 @@ spec_status_t verify_common(const uint16_t *q, const uint16_t *k_cache, const ui
     if (spec_status_t s = current_device(&dev)) return s;
 
     const int L_eff = sparse ? budget : L;
+    // the split plan numbers tiles in 32-bit arithmetic
+    if ((int64_t)B * Hkv * (((int64_t)(Hq / Hkv) * N + 63) / 64) * ((int64_t)L_eff / 64 + 1) >= ((int64_t)1 << 31))
+        return SPEC_ERR_UNSUPPORTED;
     if (ws_bytes < verify_bytes_any(B, N, Hq, Hkv, d, L_eff, dev.sms)) return SPEC_ERR_WORKSPACE;
 
     VerifyArgs a;

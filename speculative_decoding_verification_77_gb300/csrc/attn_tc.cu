@@ -75,7 +75,7 @@ __device__ __forceinline__ bool wait_bar(Bars &bs, uint64_t *bar, uint32_t parit
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 20000)) return true;  // sleeps in hardware, no spinning
         if (*(volatile uint32_t *)&bs.abort) return false;
         if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
             atomicExch(&bs.abort, 1u);
@@ -208,12 +208,17 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
     } else if (warp == WARP_MMA) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            int64_t item_base = 0;
+            uint32_t item_base = 0;
             int seg_i = 0;
             uint32_t pv_count[2] = {0, 0};   // PV MMAs issued per pipe
             uint32_t pipe_segs[2] = {0, 0};  // segments in which the pipe produced a partial
             bool ok = true;
-            const uint32_t q_base = smem_u32(sQ), ring_base = smem_u32(sRing);
+            // Descriptors are built once; every MMA only adds compile-time offsets (16-byte
+            // units), which keeps the single issuing thread's instruction stream short.
+            const uint64_t dq0 = desc_sw128(smem_u32(sQ), 16, 1024);
+            const uint64_t dq1 = split_tiles ? dq0 : dq0 + (16384u >> 4);
+            const uint64_t dk0 = desc_sw128(smem_u32(sRing), 16, 1024);
+            const uint64_t dv0 = desc_sw128(smem_u32(sRing), 16384, 1024);
             for (int64_t u = u_first; ok && u * p.tiles_per_unit < g1; ++u, ++seg_i) {
                 Seg s;
                 seg_decode(a, p, split_tiles, u, g0, g1, s);
@@ -222,42 +227,41 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
                 const int qk_total = s.cnt[0] + s.cnt[1];
                 int qk_done = 0;
                 auto issue_qk = [&](int h, int i) -> bool {
-                    const int t = seg_tile(s, split_tiles, h, i);
-                    const int64_t n = item_base + 2 * (int64_t)(t - s.tb);
-                    const int slot = (int)(n % RING);
-                    if (!wait_bar(bs, &bs.kv_full[slot], (uint32_t)((n / RING) & 1), a.status)) return false;
-                    tc_fence_after();
-                    const uint32_t qa = q_base + (split_tiles ? 0u : (uint32_t)h * 16384u);
-                    const uint32_t kb = ring_base + slot * SLOT_BYTES;
+                    const uint32_t n = item_base + 2u * (uint32_t)(seg_tile(s, split_tiles, h, i) - s.tb);
+                    const uint32_t slot = n % RING;
+                    // pipe 1 of a shared tile reuses the K tile pipe 0 already waited for
+                    if ((split_tiles || h == 0) && !wait_bar(bs, &bs.kv_full[slot], (n / RING) & 1u, a.status))
+                        return false;
+                    const uint64_t dq = h ? dq1 : dq0;
+                    const uint64_t dk = dk0 + (uint64_t)slot * (SLOT_BYTES >> 4);
+                    const uint32_t d_tmem = tmem + 128u * h;
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t off = (uint32_t)(ks >> 2) * 32768u + (uint32_t)(ks & 3) * 32u;
-                        const uint32_t offk = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
-                        mma_ss(tmem + 128u * h, desc_sw128(qa + off, 16, 1024), desc_sw128(kb + offk, 16, 1024),
-                               IDESC_QK, ks > 0);
-                    }
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_ss(d_tmem, dq + (uint64_t)((ks >> 2) * 2048 + (ks & 3) * 2),
+                               dk + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2), IDESC_QK, ks > 0 ? 1u : 0u);
                     mma_commit(&bs.s_full[h]);
                     if (split_tiles || h == 1) mma_commit(&bs.kv_empty[slot]);
                     if (++qk_done == qk_total) mma_commit(&bs.q_empty);
                     return true;
                 };
                 auto issue_pv = [&](int h, int i) -> bool {
-                    const int t = seg_tile(s, split_tiles, h, i);
                     if (!wait_bar(bs, &bs.p_full[h], pv_count[h] & 1, a.status)) return false;
                     if (i == 0 && pipe_segs[h] > 0 &&
                         !wait_bar(bs, &bs.o_empty[h], (pipe_segs[h] - 1) & 1, a.status))
                         return false;
-                    const int64_t n = item_base + 2 * (int64_t)(t - s.tb) + 1;
-                    const int slot = (int)(n % RING);
-                    if (!wait_bar(bs, &bs.kv_full[slot], (uint32_t)((n / RING) & 1), a.status)) return false;
-                    tc_fence_after();
-                    const uint32_t vb = ring_base + slot * SLOT_BYTES;
+                    const uint32_t n = item_base + 2u * (uint32_t)(seg_tile(s, split_tiles, h, i) - s.tb) + 1u;
+                    const uint32_t slot = n % RING;
+                    if ((split_tiles || h == 0) && !wait_bar(bs, &bs.kv_full[slot], (n / RING) & 1u, a.status))
+                        return false;
+                    tc_fence_after();  // P_h was written to TMEM by the softmax warps
+                    const uint64_t dv = dv0 + (uint64_t)slot * (SLOT_BYTES >> 4);
+                    const uint32_t d_tmem = tmem + 256u + 128u * h, a_tmem = tmem + 128u * h;
+                    const uint32_t acc0 = i > 0 ? 1u : 0u;
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
-                        mma_ts(tmem + 256u + 128u * h, tmem + 128u * h + 8u * ks,
-                               desc_sw128(vb + 2048u * ks, 16384, 1024), IDESC_PV, (i > 0 || ks > 0));
-                    mma_commit(&bs.o_done[h]);
+                        mma_ts(d_tmem, a_tmem + 8u * ks, dv + (uint64_t)(ks * 128), IDESC_PV, ks > 0 ? 1u : acc0);
                     if (split_tiles || h == 1) mma_commit(&bs.kv_empty[slot]);
+                    if (i == s.cnt[h] - 1) mma_commit(&bs.o_done[h]);  // the unit's O_h is final
                     ++pv_count[h];
                     return true;
                 };
@@ -272,7 +276,7 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
                     }
                 for (int h = 0; h < 2; ++h)
                     if (s.cnt[h] > 0) ++pipe_segs[h];
-                item_base += 2 * (int64_t)(s.te - s.tb);
+                item_base += 2u * (uint32_t)(s.te - s.tb);
             }
             // drain: every MMA issued so far must complete before TMEM is freed
             mma_commit(&bs.mma_done);
@@ -287,7 +291,7 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
         const uint32_t lane_addr = (uint32_t)(lg * 32) << 16;
         const uint32_t s_col = 128u * h, o_col = 256u + 128u * h;
         const float sl2 = a.scale * 1.4426950408889634f;  // scores in base 2
-        uint32_t s_count = 0, pv_signaled = 0;
+        uint32_t s_count = 0, epi_count = 0;
         bool ok = true;
         for (int64_t u = u_first; u * p.tiles_per_unit < g1; ++u) {
             Seg s;
@@ -318,15 +322,27 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
                     for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_addr + s_col + 32u * c, r[c]);
                     tmem_wait_ld();
                     const int valid = min(max(n_ctx - t * T, 0), T);  // tokens of this tile inside the context
-                    float mx = -INFINITY;
+                    if (valid < T) {  // tail tile (warp-uniform): mask the tokens past the context
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
+                        for (int c = 0; c < 4; ++c)
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const float x = (32 * c + j < valid) ? __uint_as_float(r[c][j]) * sl2 : -INFINITY;
-                            r[c][j] = __float_as_uint(x);
-                            mx = fmaxf(mx, x);
-                        }
+                            for (int j = 0; j < 32; ++j)
+                                if (32 * c + j >= valid) r[c][j] = __float_as_uint(-INFINITY);
+                    }
+                    // row max of the raw scores (scale > 0): eight independent chains of
+                    // three-operand max, then a short tree
+                    float mx8[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        mx8[q] = fmaxf(__uint_as_float(r[q >> 1][(q & 1) * 16]), __uint_as_float(r[q >> 1][(q & 1) * 16 + 1]));
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+#pragma unroll
+                        for (int j = 2; j < 16; j += 2)
+                            mx8[q] = fmax3(mx8[q], __uint_as_float(r[q >> 1][(q & 1) * 16 + j]),
+                                           __uint_as_float(r[q >> 1][(q & 1) * 16 + j + 1]));
+                    float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+                    mx *= sl2;  // base-2 units
                     // move the reference max only when it grows by more than 2^8
                     bool rescale_o = false;
                     float factor = 1.f;
@@ -336,49 +352,54 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
                         l *= factor;
                         m_ref = mx;
                     }
-                    if (__any_sync(0xffffffffu, rescale_o) && k > 0) {
-                        // O holds the previous tiles: wait for their PV, then rescale this warp's rows
-                        ok = __all_sync(0xffffffffu, ok && wait_bar(bs, &bs.o_done[h], (pv_signaled - 1) & 1, a.status));
-                        tc_fence_after();
-                        if (ok) {
-                            const float f = rescale_o ? factor : 1.f;
-#pragma unroll 1
-                            for (int c = 0; c < 4; ++c) {
-                                uint32_t o[32];
-                                tmem_ld32(tmem + lane_addr + o_col + 32u * c, o);
-                                tmem_wait_ld();
-#pragma unroll
-                                for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
-                                tmem_st32(tmem + lane_addr + o_col + 32u * c, o);
-                            }
-                            tmem_wait_st();
-                        }
-                    }
+                    // p = 2^(s * sl2 - m_ref), two columns per fp32x2 instruction
                     const float mref = m_ref == -INFINITY ? 0.f : m_ref;
-                    float sum = 0.f;
+                    const uint64_t scale2 = pack2(sl2, sl2), shift2 = pack2(-mref, -mref);
+                    uint64_t sum2[4] = {pack2(0.f, 0.f), pack2(0.f, 0.f), pack2(0.f, 0.f), pack2(0.f, 0.f)};
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint32_t pk[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
-                            const float p0 = ex2(__uint_as_float(r[c][2 * j]) - mref);
-                            const float p1 = ex2(__uint_as_float(r[c][2 * j + 1]) - mref);
-                            sum += p0 + p1;
+                            float x0, x1;
+                            unpack2(ffma2(pack2(__uint_as_float(r[c][2 * j]), __uint_as_float(r[c][2 * j + 1])),
+                                          scale2, shift2),
+                                    x0, x1);
+                            const float p0 = ex2(x0), p1 = ex2(x1);
+                            sum2[j & 3] = fadd2(sum2[j & 3], pack2(p0, p1));
                             __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
                             pk[j] = *reinterpret_cast<uint32_t *>(&v);
                         }
                         tmem_st16(tmem + lane_addr + s_col + 16u * c, pk);
                     }
-                    l += sum;
+                    float sa, sb;
+                    unpack2(fadd2(fadd2(sum2[0], sum2[1]), fadd2(sum2[2], sum2[3])), sa, sb);
+                    l += sa + sb;
                     tmem_wait_st();
+                    if (__any_sync(0xffffffffu, rescale_o) && k > 0) {
+                        // O holds the previous tiles. Their PV has completed: the commit that
+                        // signalled this S_h came after it from the same issuing thread. Rescale
+                        // this warp's rows (after P is built, so the score registers are free).
+                        const float f = rescale_o ? factor : 1.f;
+#pragma unroll 1
+                        for (int c = 0; c < 4; ++c) {
+                            uint32_t o[32];
+                            tmem_ld32(tmem + lane_addr + o_col + 32u * c, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
+                            tmem_st32(tmem + lane_addr + o_col + 32u * c, o);
+                        }
+                        tmem_wait_st();
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bs.p_full[h]);
-                ++pv_signaled;
             }
             // epilogue: O / l and lse of this pipe's rows -> partial slot
-            ok = __all_sync(0xffffffffu, ok && wait_bar(bs, &bs.o_done[h], (pv_signaled - 1) & 1, a.status));
+            ok = __all_sync(0xffffffffu, ok && wait_bar(bs, &bs.o_done[h], epi_count & 1, a.status));
+            ++epi_count;
             tc_fence_after();
             if (ok && warp_rows) {
                 const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -434,7 +455,8 @@ bool encode_map(CUtensorMap *map, const void *base, int rank, const cuuint64_t *
 }  // namespace
 
 bool tc_supported(const VerifyArgs &a) {
-    return a.L >= 1 && a.G >= 1 && a.G <= 128 && (128 % a.G) == 0 && !a.idx;
+    // the softmax takes the row max of the raw scores, which needs scale > 0
+    return a.L >= 1 && a.G >= 1 && a.G <= 128 && (128 % a.G) == 0 && !a.idx && a.scale > 0.f;
 }
 
 cudaError_t launch_cache_attn_tc(const VerifyArgs &a, const SplitPlan &p, cudaStream_t s, cudaEvent_t ev0,

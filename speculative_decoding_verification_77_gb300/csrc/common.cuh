@@ -41,13 +41,19 @@ struct SplitPlan {
     int slot_rows;      // rows per slot
     int split_tiles;    // 1: the pipes cover alternate tiles of the same rows (both slots per row);
                         // 0: pipe h covers rows [h*slot_rows, (h+1)*slot_rows) of the unit
+    int q, rem;         // total = q * ctas + rem
 };
 
+// CTA c covers q or q+1 tiles: the first `rem` CTAs take q+1 (q = total / ctas,
+// rem = total % ctas). All in 32-bit arithmetic (total < 2^31 is checked on the host).
 __host__ __device__ __forceinline__ int64_t plan_start(const SplitPlan &p, int64_t c) {
-    return c * p.total / p.ctas;
+    const int ci = (int)c;
+    return (int64_t)ci * p.q + (ci < p.rem ? ci : p.rem);
 }
 __host__ __device__ __forceinline__ int64_t plan_cta_of(const SplitPlan &p, int64_t g) {
-    return ((g + 1) * (int64_t)p.ctas - 1) / p.total;
+    const int gi = (int)g;
+    const int big = p.rem * (p.q + 1);
+    return gi < big ? gi / (p.q + 1) : p.rem + (gi - big) / p.q;
 }
 
 inline SplitPlan make_plan(int B, int N, int Hq, int Hkv, int L_eff, int BM, int tile, int max_ctas) {
@@ -61,6 +67,8 @@ inline SplitPlan make_plan(int B, int N, int Hq, int Hkv, int L_eff, int BM, int
     p.total = (int64_t)p.units * p.tiles_per_unit;
     p.ctas = (int)(p.total < max_ctas ? p.total : max_ctas);
     if (p.ctas < 1) p.ctas = 1;
+    p.q = (int)(p.total / p.ctas);
+    p.rem = (int)(p.total % p.ctas);
     p.pipes = 1;
     p.slot_rows = BM;
     p.split_tiles = 0;

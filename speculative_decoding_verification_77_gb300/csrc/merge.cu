@@ -8,26 +8,6 @@ namespace specverify {
 
 namespace {
 
-struct OnlineRow {
-    float m = -INFINITY;  // running max of the natural-log weights
-    float s = 0.f;        // running sum of exp(weight - m)
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-
-    // add a term exp(w) * x (x = 4 components of the row held by this lane)
-    __device__ __forceinline__ void add(float w, float4 x) {
-        if (w == -INFINITY) return;
-        if (w > m) {
-            float c = __expf(m - w);  // m == -inf -> 0
-            acc.x *= c; acc.y *= c; acc.z *= c; acc.w *= c;
-            s *= c;
-            m = w;
-        }
-        float e = __expf(w - m);
-        acc.x += e * x.x; acc.y += e * x.y; acc.z += e * x.z; acc.w += e * x.w;
-        s += e;
-    }
-};
-
 __device__ __forceinline__ float4 load_bf16x4(const __nv_bfloat16 *p) {
     uint2 u = *reinterpret_cast<const uint2 *>(p);
     __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162 *>(&u.x);
@@ -36,61 +16,122 @@ __device__ __forceinline__ float4 load_bf16x4(const __nv_bfloat16 *p) {
     return make_float4(fa.x, fa.y, fb.x, fb.y);
 }
 
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
 }
 
+// Running log-sum-exp state of a warp, fed in batches of up to 32 terms: lane d
+// holds the natural-log weight of term d of the batch; a term's row (4 columns
+// per lane) is loaded once its weight is known, and the loads of a batch are
+// independent, so they are in flight together.
+struct WarpLse {
+    float m = -INFINITY, s = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+
+    // folds the batch max into m; returns this lane's weight exp(w - m)
+    __device__ __forceinline__ float begin_batch(float w) {
+        const float bm = warp_max(w);
+        if (bm > m) {
+            const float c = __expf(m - bm);  // m == -inf -> 0
+            acc.x *= c; acc.y *= c; acc.z *= c; acc.w *= c;
+            s *= c;
+            m = bm;
+        }
+        const float e = w == -INFINITY ? 0.f : __expf(w - m);
+        s += warp_sum(e);
+        return e;
+    }
+    __device__ __forceinline__ void add(float e, float4 x) {
+        acc.x += e * x.x; acc.y += e * x.y; acc.z += e * x.z; acc.w += e * x.w;
+    }
+};
+
 // One warp per output row (b, i, h); lane holds columns 4*lane .. 4*lane+3.
+// Terms: (a) the normalised partials of every CTA and pipe that covered the
+// row's unit, weighted by their lse; (b) the draft keys the tree mask lets the
+// row see (node i and its ancestors), weighted by their logits.
 __global__ void __launch_bounds__(256) merge_tree_kernel(VerifyArgs a, SplitPlan p) {
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t rows = (int64_t)a.B * a.N * a.Hq;
+    const int rows = a.B * a.N * a.Hq;
     if (warp >= rows) return;
     const int h = warp % a.Hq;
-    const int i = (warp / a.Hq) % a.N;
-    const int b = warp / (a.Hq * a.N);
-    const int hk = h / a.G, g = h % a.G;
+    const int bi = warp / a.Hq;  // b * N + i
+    const int i = bi % a.N, b = bi / a.N;
+    const int hk = h / a.G, g = h - hk * a.G;
     const int rfull = i * a.G + g;
-    const int rg = rfull / p.BM, ru = rfull % p.BM;
-    const int64_t u = ((int64_t)b * a.Hkv + hk) * p.row_groups + rg;
+    const int rg = rfull / p.BM, ru = rfull - rg * p.BM;
+    const int u = (b * a.Hkv + hk) * p.row_groups + rg;
     // which pipe slots hold this row, and the row inside a slot
     const int h_lo = p.split_tiles ? 0 : ru / p.slot_rows;
-    const int h_hi = p.split_tiles ? p.pipes - 1 : h_lo;
+    const int nh_shift = p.split_tiles && p.pipes == 2 ? 1 : 0;  // one or two pipe slots per CTA
     const int r = p.split_tiles ? ru : ru % p.slot_rows;
+    const int c_lo = (int)plan_cta_of(p, (int64_t)u * p.tiles_per_unit);
+    const int c_hi = (int)plan_cta_of(p, (int64_t)(u + 1) * p.tiles_per_unit - 1);
+    const int n_parts = (c_hi - c_lo + 1) << nh_shift;
+    const int64_t row0 = ((int64_t)(c_lo + u) * p.pipes + h_lo) * p.slot_rows + r;
+    const int64_t cta_stride = (int64_t)p.pipes * p.slot_rows;
 
-    OnlineRow st;
-    // cache part: the normalised partials of every CTA (and pipe) that covered this unit
-    const int64_t c_lo = plan_cta_of(p, u * p.tiles_per_unit);
-    const int64_t c_hi = plan_cta_of(p, (u + 1) * p.tiles_per_unit - 1);
-    for (int64_t c = c_lo; c <= c_hi; ++c) {
-        for (int hh = h_lo; hh <= h_hi; ++hh) {
-            const int64_t slot = (c + u) * p.pipes + hh;
-            const float w = a.lse_part[slot * p.slot_rows + r];
-            const float4 o =
-                *reinterpret_cast<const float4 *>(a.o_part + (slot * p.slot_rows + r) * kHeadDim + 4 * lane);
-            st.add(w, o);
+    WarpLse st;
+    // (a) cache part
+    for (int k0 = 0; k0 < n_parts; k0 += 32) {
+        const int nb = min(32, n_parts - k0);
+        const int k = k0 + lane;
+        const float w = lane < nb ? a.lse_part[row0 + (k >> nh_shift) * cta_stride + (k & nh_shift) * p.slot_rows]
+                                  : -INFINITY;
+        const float e = st.begin_batch(w);
+#pragma unroll 4
+        for (int d = 0; d < nb; ++d) {
+            const float ed = __shfl_sync(0xffffffffu, e, d);
+            const int kd = k0 + d;
+            const int64_t row = row0 + (kd >> nh_shift) * cta_stride + (kd & nh_shift) * p.slot_rows;
+            if (ed != 0.f) st.add(ed, *reinterpret_cast<const float4 *>(a.o_part + row * kHeadDim + 4 * lane));
         }
     }
-    // speculative part: node i and its ancestors (tree mask)
+    // (b) speculative part, walking node i's ancestors 32 at a time
     if (a.k_draft) {
-        const float4 qv = load_bf16x4(a.q + (((int64_t)b * a.N + i) * a.Hq + h) * kHeadDim + 4 * lane);
+        const float4 qv = load_bf16x4(a.q + (int64_t)warp * kHeadDim + 4 * lane);
         const int32_t *par = a.parent + (int64_t)b * a.N;
+        const int64_t node_stride = (int64_t)a.Hkv * kHeadDim;
+        const __nv_bfloat16 *kd = a.k_draft + ((int64_t)b * a.N * a.Hkv + hk) * kHeadDim + 4 * lane;
+        const __nv_bfloat16 *vd = a.v_draft + ((int64_t)b * a.N * a.Hkv + hk) * kHeadDim + 4 * lane;
         int j = i;
-        while (true) {
-            const int64_t kv_off = (((int64_t)b * a.N + j) * a.Hkv + hk) * kHeadDim + 4 * lane;
-            const float4 kv = load_bf16x4(a.k_draft + kv_off);
-            float dot = qv.x * kv.x + qv.y * kv.y + qv.z * kv.z + qv.w * kv.w;
-            dot = warp_sum(dot);
-            st.add(dot * a.scale, load_bf16x4(a.v_draft + kv_off));
-            const int pj = __ldg(par + j);
-            if (pj == -1) break;
-            if (pj < -1 || pj >= j) {  // not a tree in topological order: stop here
-                if (lane == 0) flag_status(a.status, SPEC_ERR_BAD_INPUT);
-                break;
+        while (j >= 0) {
+            int mine = -1, nb = 0;
+            while (nb < 32 && j >= 0) {  // lane nb records the next ancestor
+                if (lane == nb) mine = j;
+                ++nb;
+                const int pj = __ldg(par + j);
+                if (pj < -1 || pj >= j) {  // not a tree in topological order: stop here
+                    if (lane == 0) flag_status(a.status, SPEC_ERR_BAD_INPUT);
+                    j = -1;
+                } else {
+                    j = pj;
+                }
             }
-            j = pj;
+            float logit = -INFINITY;
+#pragma unroll 4
+            for (int d = 0; d < nb; ++d) {
+                const int node = __shfl_sync(0xffffffffu, mine, d);
+                const float4 kv = load_bf16x4(kd + node * node_stride);
+                const float dot = warp_sum(qv.x * kv.x + qv.y * kv.y + qv.z * kv.z + qv.w * kv.w) * a.scale;
+                if (lane == d) logit = dot;
+            }
+            const float e = st.begin_batch(logit);
+#pragma unroll 4
+            for (int d = 0; d < nb; ++d) {
+                const float ed = __shfl_sync(0xffffffffu, e, d);
+                const int node = __shfl_sync(0xffffffffu, mine, d);
+                st.add(ed, load_bf16x4(vd + node * node_stride));
+            }
         }
     }
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
