@@ -207,7 +207,9 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
         __syncwarp();
     } else if (warp == WARP_MMA) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs the issue loop (its operands stay warp-uniform); one elected
+        // lane issues each tcgen05 instruction.
+        {
             uint32_t item_base = 0;
             int seg_i = 0;
             uint32_t pv_count[2] = {0, 0};   // PV MMAs issued per pipe
@@ -222,7 +224,7 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
             for (int64_t u = u_first; ok && u * p.tiles_per_unit < g1; ++u, ++seg_i) {
                 Seg s;
                 seg_decode(a, p, split_tiles, u, g0, g1, s);
-                if (!(ok = wait_bar(bs, &bs.q_full, seg_i & 1, a.status))) break;
+                if (!(ok = __all_sync(0xffffffffu, wait_bar(bs, &bs.q_full, seg_i & 1, a.status)))) break;
                 tc_fence_after();
                 const int qk_total = s.cnt[0] + s.cnt[1];
                 int qk_done = 0;
@@ -230,28 +232,28 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
                     const uint32_t n = item_base + 2u * (uint32_t)(seg_tile(s, split_tiles, h, i) - s.tb);
                     const uint32_t slot = n % RING;
                     // pipe 1 of a shared tile reuses the K tile pipe 0 already waited for
-                    if ((split_tiles || h == 0) && !wait_bar(bs, &bs.kv_full[slot], (n / RING) & 1u, a.status))
+                    if ((split_tiles || h == 0) && !__all_sync(0xffffffffu, wait_bar(bs, &bs.kv_full[slot], (n / RING) & 1u, a.status)))
                         return false;
                     const uint64_t dq = h ? dq1 : dq0;
                     const uint64_t dk = dk0 + (uint64_t)slot * (SLOT_BYTES >> 4);
                     const uint32_t d_tmem = tmem + 128u * h;
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
-                        mma_ss(d_tmem, dq + (uint64_t)((ks >> 2) * 2048 + (ks & 3) * 2),
+                        mma_ss_elect(d_tmem, dq + (uint64_t)((ks >> 2) * 2048 + (ks & 3) * 2),
                                dk + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2), IDESC_QK, ks > 0 ? 1u : 0u);
-                    mma_commit(&bs.s_full[h]);
-                    if (split_tiles || h == 1) mma_commit(&bs.kv_empty[slot]);
-                    if (++qk_done == qk_total) mma_commit(&bs.q_empty);
+                    mma_commit_elect(&bs.s_full[h]);
+                    if (split_tiles || h == 1) mma_commit_elect(&bs.kv_empty[slot]);
+                    if (++qk_done == qk_total) mma_commit_elect(&bs.q_empty);
                     return true;
                 };
                 auto issue_pv = [&](int h, int i) -> bool {
-                    if (!wait_bar(bs, &bs.p_full[h], pv_count[h] & 1, a.status)) return false;
+                    if (!__all_sync(0xffffffffu, wait_bar(bs, &bs.p_full[h], pv_count[h] & 1, a.status))) return false;
                     if (i == 0 && pipe_segs[h] > 0 &&
-                        !wait_bar(bs, &bs.o_empty[h], (pipe_segs[h] - 1) & 1, a.status))
+                        !__all_sync(0xffffffffu, wait_bar(bs, &bs.o_empty[h], (pipe_segs[h] - 1) & 1, a.status)))
                         return false;
                     const uint32_t n = item_base + 2u * (uint32_t)(seg_tile(s, split_tiles, h, i) - s.tb) + 1u;
                     const uint32_t slot = n % RING;
-                    if ((split_tiles || h == 0) && !wait_bar(bs, &bs.kv_full[slot], (n / RING) & 1u, a.status))
+                    if ((split_tiles || h == 0) && !__all_sync(0xffffffffu, wait_bar(bs, &bs.kv_full[slot], (n / RING) & 1u, a.status)))
                         return false;
                     tc_fence_after();  // P_h was written to TMEM by the softmax warps
                     const uint64_t dv = dv0 + (uint64_t)slot * (SLOT_BYTES >> 4);
@@ -259,9 +261,9 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
                     const uint32_t acc0 = i > 0 ? 1u : 0u;
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
-                        mma_ts(d_tmem, a_tmem + 8u * ks, dv + (uint64_t)(ks * 128), IDESC_PV, ks > 0 ? 1u : acc0);
-                    if (split_tiles || h == 1) mma_commit(&bs.kv_empty[slot]);
-                    if (i == s.cnt[h] - 1) mma_commit(&bs.o_done[h]);  // the unit's O_h is final
+                        mma_ts_elect(d_tmem, a_tmem + 8u * ks, dv + (uint64_t)(ks * 128), IDESC_PV, ks > 0 ? 1u : acc0);
+                    if (split_tiles || h == 1) mma_commit_elect(&bs.kv_empty[slot]);
+                    if (i == s.cnt[h] - 1) mma_commit_elect(&bs.o_done[h]);  // the unit's O_h is final
                     ++pv_count[h];
                     return true;
                 };
@@ -279,10 +281,9 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
                 item_base += 2u * (uint32_t)(s.te - s.tb);
             }
             // drain: every MMA issued so far must complete before TMEM is freed
-            mma_commit(&bs.mma_done);
+            mma_commit_elect(&bs.mma_done);
             drain_wait(&bs.mma_done, 0);
         }
-        __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax warps
         const int h = warp >> 2;            // pipe
