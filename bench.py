@@ -127,12 +127,40 @@ class ClockSampler:
 # native arm
 
 
+def oracle_select_seconds(x) -> float:
+    """Seconds the CPU oracle takes for the whole selection of a sparse workload (0 if dense)."""
+    import oracle
+
+    w = x["workload"]
+    if not w.sparse:
+        return 0.0
+    t = time.perf_counter()
+    oracle.select(x["draft_score"], x["target_score"], sink=w.sink, window=w.window, top_m=w.top_m,
+                  budget=w.budget)
+    return time.perf_counter() - t
+
+
+def oracle_rows(x, rows, idx):
+    import oracle
+
+    oracle.attend(x["q"], x["k_cache"], x["v_cache"], x["k_draft"], x["v_draft"], x["parent"],
+                  scale=x["scale"], rows=rows, idx=idx)
+
+
 def oracle_baseline(x, rows_target_s: float = 10.0, max_rows: int | None = None):
-    """Time the CPU oracle (as it stands) on a sample of rows; extrapolate to one step."""
+    """Time the CPU oracle (as it stands) on a sample of rows; extrapolate to one step.
+
+    A sparse step is the oracle selection of every sequence (timed whole) plus
+    sparse attention over the chosen indices (timed on sampled rows)."""
     import oracle
 
     w = x["workload"]
     total_rows = w.B * w.N * w.Hq
+    sel_s = oracle_select_seconds(x)
+    idx = None
+    if w.sparse:
+        idx = oracle.select(x["draft_score"], x["target_score"], sink=w.sink, window=w.window,
+                            top_m=w.top_m, budget=w.budget)[0]
     rng = np.random.default_rng(0)
     n = 16
     elapsed = 0.0
@@ -140,18 +168,18 @@ def oracle_baseline(x, rows_target_s: float = 10.0, max_rows: int | None = None)
     while True:
         rows = rng.choice(total_rows, size=min(n, total_rows - done), replace=False)
         t = time.perf_counter()
-        oracle.attend(x["q"], x["k_cache"], x["v_cache"], x["k_draft"], x["v_draft"], x["parent"],
-                      scale=x["scale"], rows=rows)
+        oracle_rows(x, rows, idx)
         dt = time.perf_counter() - t
         elapsed += dt
         done += len(rows)
         if elapsed >= rows_target_s or done >= total_rows or (max_rows and done >= max_rows):
             break
         n = min(total_rows, max(n, int(len(rows) * (rows_target_s - elapsed) / max(dt, 1e-3))))
-    step_s = elapsed / done * total_rows
+    step_s = sel_s + elapsed / done * total_rows
     cores = len(os.sched_getaffinity(0))
+    sel = f"selection of all {w.B} sequences {sel_s:.2f} s + " if w.sparse else ""
     return {"value": w.kv_bytes() / step_s / 1e12, "unit": "TB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{done} of {total_rows} output rows (fp64, OpenMP over rows), {elapsed:.1f} s, "
+            "sample": f"{sel}{done} of {total_rows} output rows (fp64, OpenMP over rows), {elapsed:.1f} s, "
                       f"extrapolated to one step: {step_s:.2f} s/step"}
 
 
@@ -163,52 +191,78 @@ def run_native(args, ws_, rank, local):
     w = W.workload(args.workload)
     x = W.make_inputs(w)
     names = ["q", "k_cache", "v_cache", "k_draft", "v_draft", "parent"]
+    if w.sparse:
+        names += ["draft_score", "target_score"]
     host = {k: x[k].pin_memory() for k in names}
     g = {k: host[k].to(dev, non_blocking=True) for k in names}
     torch.cuda.synchronize()
     scale = x["scale"]
     out = torch.empty((w.B, w.N, w.Hq, w.d), dtype=torch.float32, device=dev)
     lse = torch.empty((w.B, w.N, w.Hq), dtype=torch.float32, device=dev)
+    idx = torch.empty((w.B, max(w.budget, 1)), dtype=torch.int32, device=dev)
+    cnt = torch.empty((w.B,), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
-        ops.verify_attn(g["q"], g["k_cache"], g["v_cache"], g["k_draft"], g["v_draft"], g["parent"],
-                        scale=scale, out=out, lse=lse)
+    def step(t):
+        if w.sparse:
+            ops.select_topk(t["draft_score"], t["target_score"], sink=w.sink, window=w.window, top_m=w.top_m,
+                            budget=w.budget, idx=idx, count=cnt)
+            return ops.verify_attn_sparse(t["q"], t["k_cache"], t["v_cache"], t["k_draft"], t["v_draft"],
+                                          t["parent"], idx, scale=scale, out=out, lse=lse)
+        return ops.verify_attn(t["q"], t["k_cache"], t["v_cache"], t["k_draft"], t["v_draft"], t["parent"],
+                               scale=scale, out=out, lse=lse)
+
+    # Inputs read per step smaller than 4x L2 (the sparse gather, the tiny case) get an L2 flush
+    # before every step, outside the step's events; larger ones stream from HBM anyway.
+    flush = w.kv_bytes() < 4 * L2_BYTES
+    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
 
     for _ in range(args.warmup):
-        step()
+        step(g)
     torch.cuda.synchronize()
-    kd_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-             for _ in range(args.steps)]
-    for a, b in kd_ev:  # materialise the events before handing them to the library
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    kd_ev = [(ev(), ev()) for _ in range(args.steps)]
+    st_ev = [(ev(), ev()) for _ in range(args.steps)]
+    for a, b in kd_ev + st_ev:  # materialise the events before handing them to the library
         a.record(stream)
         b.record(stream)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
     barrier(ws_)
     torch.cuda.synchronize()
     launches0 = ops.kernel_launches()
     t0 = time.time()
-    ev0.record(stream)
     for i in range(args.steps):
+        if flush:
+            scratch.fill_(float(i))
+        st_ev[i][0].record(stream)
+        step(g)
+        st_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    launches = ops.kernel_launches() - launches0
+    # The cache kernel's own duration, from a second pass of K steps with CUDA events that
+    # the library records around that launch. An event between the cache kernel and the
+    # merge stops the merge from starting early (programmatic dependent launch), so these
+    # events stay out of the pass that gives the step time.
+    for i in range(args.steps):
+        if flush:
+            scratch.fill_(float(i))
         ops.profile_events(*kd_ev[i])
-        step()
-    ev1.record(stream)
+        step(g)
     ops.profile_events(None, None)
     torch.cuda.synchronize()
     t1 = time.time()
     barrier(ws_)
-    launches = ops.kernel_launches() - launches0
     clocks.stop()
-    ms = ev0.elapsed_time(ev1) / args.steps
+    ms = sum(a.elapsed_time(b) for a, b in st_ev) / args.steps
     kd_ms = sum(a.elapsed_time(b) for a, b in kd_ev) / args.steps
     ms_max = allreduce_max(ws_, ms, dev)
 
     # end to end through the public API: pinned host inputs -> device, verify, result -> host
     if args.no_e2e:
         e2e_ms = float("nan")
-        return finish(args, ws_, rank, w, ms, ms_max, kd_ms, launches, None, None, e2e_ms, clocks, t0, t1, x)
+        return finish(args, ws_, rank, w, ms, ms_max, kd_ms, launches, None, None, e2e_ms, clocks, t0, t1, x,
+                      flush)
     dbuf = {k: torch.empty_like(g[k]) for k in names}
     hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     hlse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
@@ -218,8 +272,7 @@ def run_native(args, ws_, rank, local):
     def e2e_step():
         for k in names:
             dbuf[k].copy_(host[k], non_blocking=True)
-        o, l_ = ops.verify_attn(dbuf["q"], dbuf["k_cache"], dbuf["v_cache"], dbuf["k_draft"], dbuf["v_draft"],
-                                dbuf["parent"], scale=scale, out=out, lse=lse)
+        o, l_ = step(dbuf)
         hout.copy_(o, non_blocking=True)
         hlse.copy_(l_, non_blocking=True)
 
@@ -227,17 +280,17 @@ def run_native(args, ws_, rank, local):
         e2e_step()
     torch.cuda.synchronize()
     barrier(ws_)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0, e1 = ev(), ev()
     e0.record(stream)
     for _ in range(args.steps):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = allreduce_max(ws_, e0.elapsed_time(e1) / args.steps, dev)
-    return finish(args, ws_, rank, w, ms, ms_max, kd_ms, launches, h2d, d2h, e2e_ms, clocks, t0, t1, x)
+    return finish(args, ws_, rank, w, ms, ms_max, kd_ms, launches, h2d, d2h, e2e_ms, clocks, t0, t1, x, flush)
 
 
-def finish(args, ws_, rank, w, ms, ms_max, kd_ms, launches, h2d, d2h, e2e_ms, clocks, t0, t1, x):
+def finish(args, ws_, rank, w, ms, ms_max, kd_ms, launches, h2d, d2h, e2e_ms, clocks, t0, t1, x, flush):
     if rank != 0:
         return None
     peaks, peak_src = measured_peaks()
@@ -257,15 +310,14 @@ def finish(args, ws_, rank, w, ms, ms_max, kd_ms, launches, h2d, d2h, e2e_ms, cl
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) bf16 Q/K/V, random draft tree)",
-        "config": {"workload": w.name, "B": w.B, "L": w.L, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "N": w.N,
-                   "tree": f"{w.tree} depth<={w.depth_max}", "kv_bytes_per_step": kv,
-                   "l2": "inputs larger than L2 (K/V 512 MiB vs 129 MB), no flush",
-                   "parallelism": f"replicas x{ws_}"},
-        "roofline": {"bound": "hbm", "kernel": "cache_attn_tc (tcgen05 split-KV)", "achieved": round(achieved_gbs, 1),
+        "data": "synthetic (seeded N(0,1) bf16 Q/K/V, " + ("softmax(4z) scores, " if w.sparse else "") +
+                f"{w.tree} draft tree)",
+        "config": config_of(w, ws_, kv, flush),
+        "roofline": {"bound": "hbm", "kernel": kernel_name(w), "achieved": round(achieved_gbs, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved_gbs / peaks["hbm_gbs"], 4),
                      "peak_source": f"{peak_src} copy bandwidth", "traffic": traffic,
-                     "kernel_ms": round(kd_ms, 5), "share_of_step": round(kd_ms / ms, 4)},
+                     "kernel_ms": round(kd_ms, 5), "share_of_step": round(kd_ms / ms, 4),
+                     "timing": "CUDA events around each cache-kernel launch, launching stream, second pass of K steps"},
         "gpu_launches": int(launches),
         "e2e": None if h2d is None else {
             "value": round(kv / (e2e_ms * 1e-3) / 1e12, 4), "unit": "TB/s", "ms_per_step": round(e2e_ms, 4),
@@ -275,6 +327,26 @@ def finish(args, ws_, rank, w, ms, ms_max, kd_ms, launches, h2d, d2h, e2e_ms, cl
     if ws_ == 1 and not args.no_cpu_baseline:  # the CPU baseline is taken on rank 0 at N=1 only
         rec["cpu_baseline"] = oracle_baseline(x, rows_target_s=args.cpu_seconds)
     return rec
+
+
+def config_of(w, ws_, kv, flush):
+    c = {"workload": w.name, "B": w.B, "L": w.L, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "N": w.N,
+         "tree": w.tree + (f" depth<={w.depth_max}" if w.tree == "random" else ""), "kv_bytes_per_step": kv,
+         "l2": (f"L2 flushed before every step ({2 * L2_BYTES >> 20} MiB write, outside the step events)" if flush
+                else f"inputs larger than L2 (K/V {kv >> 20} MiB vs 129 MB), no flush"),
+         "parallelism": f"replicas x{ws_}"}
+    if w.sparse:
+        c.update(sink=w.sink, window=w.window, top_m=w.top_m, budget=w.budget,
+                 step="spec_select_topk + spec_verify_attn_sparse")
+    else:
+        c["step"] = "spec_verify_attn"
+    return c
+
+
+def kernel_name(w):
+    if w.sparse:
+        return "cache_attn_mma<sparse> (mma.sync index gather)"
+    return "cache_attn_tc (tcgen05 split-KV)"
 
 
 def barrier(ws_):
@@ -304,9 +376,14 @@ def run_reference(args, ws_, rank):
     rng = np.random.default_rng(1)
     import oracle
 
+    idx = None
+    if w.sparse:
+        idx = oracle.select(x["draft_score"], x["target_score"], sink=w.sink, window=w.window,
+                            top_m=w.top_m, budget=w.budget)[0]
+    sel_s = oracle_select_seconds(x)
+
     def one(rows):
-        oracle.attend(x["q"], x["k_cache"], x["v_cache"], x["k_draft"], x["v_draft"], x["parent"],
-                      scale=x["scale"], rows=rows)
+        oracle_rows(x, rows, idx)
 
     for _ in range(args.warmup):
         one(rng.choice(total_rows, size=per_step_rows, replace=False))
@@ -314,15 +391,18 @@ def run_reference(args, ws_, rank):
     for _ in range(args.steps):
         one(rng.choice(total_rows, size=per_step_rows, replace=False))
     el = time.perf_counter() - t
-    step_s = el / (args.steps * per_step_rows) * total_rows
+    step_s = sel_s + el / (args.steps * per_step_rows) * total_rows
     value = w.kv_bytes() / step_s / 1e12
     cores = len(os.sched_getaffinity(0))
     sample = f"{per_step_rows} of {total_rows} output rows per step, extrapolated to the full step"
+    if w.sparse:
+        sample += f", plus the selection of all {w.B} sequences ({sel_s:.2f} s)"
     return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TB/s", "n_gpus": ws_,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": w.name, "B": w.B, "L": w.L, "Hq": w.Hq, "Hkv": w.Hkv,
-                                            "d": w.d, "N": w.N, "parallelism": "host cores (OpenMP)"},
+            "data": "synthetic",
+            "config": dict(config_of(w, ws_, w.kv_bytes(), False), l2="n/a (CPU)",
+                           parallelism="host cores (OpenMP)"),
             "cpu_baseline": {"value": round(value, 6), "unit": "TB/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

@@ -84,6 +84,7 @@ __device__ __forceinline__ int cache_token(const VerifyArgs &a, int b, int n, in
 
 template <bool SPARSE>
 __global__ void __launch_bounds__(THREADS, 2) cache_attn_mma_kernel(VerifyArgs a, SplitPlan p) {
+    griddep_launch_dependents();  // the merge may be scheduled as this grid's CTAs drain
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *sQ = smem;
     uint8_t *sKV = smem + BM * D * 2;  // [stage][K|V][BN][D]

@@ -122,6 +122,7 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
                      const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v) {
     extern __shared__ uint8_t smem_raw[];
+    griddep_launch_dependents();  // the merge may be scheduled as this grid's CTAs drain
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint8_t *sQ = smem;
     uint8_t *sRing = smem + SMEM_RING;

@@ -13,6 +13,16 @@ constexpr int kHeadDim = 128;
 constexpr size_t kHeaderBytes = 256;  // status word + reserved, at the start of every workspace
 
 // Status word handling (device side). Never traps: the most severe code wins.
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start before the previous kernel on the
+// stream ends; griddepcontrol.wait blocks until that kernel has completed and
+// its writes are visible. launch_dependents lets the dependent grid be
+// scheduled once every CTA of this grid has issued it (or exited).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void flag_status(uint32_t *status, uint32_t code) {
     if (status) atomicMax(status, code);
 }

@@ -16,61 +16,156 @@ __device__ __forceinline__ float4 load_bf16x4(const __nv_bfloat16 *p) {
     return make_float4(fa.x, fa.y, fb.x, fb.y);
 }
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
 }
 
-// Running log-sum-exp state of a warp, fed in batches of up to 32 terms: lane d
-// holds the natural-log weight of term d of the batch; a term's row (4 columns
-// per lane) is loaded once its weight is known, and the loads of a batch are
-// independent, so they are in flight together.
-struct WarpLse {
-    float m = -INFINITY, s = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+// Reductions over the lanes that hold the same row j = lane % GB (lane bits >= log2 GB).
+template <int GB>
+__device__ __forceinline__ float group_max(float v) {
+#pragma unroll
+    for (int o = 16; o >= GB; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+template <int GB>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+    for (int o = 16; o >= GB; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
 
-    // folds the batch max into m; returns this lane's weight exp(w - m)
-    __device__ __forceinline__ float begin_batch(float w) {
-        const float bm = warp_max(w);
-        if (bm > m) {
-            const float c = __expf(m - bm);  // m == -inf -> 0
-            acc.x *= c; acc.y *= c; acc.z *= c; acc.w *= c;
-            s *= c;
-            m = bm;
+// Running log-sum-exp state of GB rows held by one warp (lane holds columns
+// 4*lane .. 4*lane+3 of every row). Terms arrive in batches of up to 32/GB:
+// lane q holds the natural-log weight of term q / GB for row q % GB.
+template <int GB>
+struct RowsLse {
+    float m[GB], s[GB];  // warp-uniform running max and sum of every row
+    float4 acc[GB];
+    float m_mine;        // m[lane % GB], kept in step without indexing m by a lane-dependent value
+    __device__ __forceinline__ RowsLse() : m_mine(-INFINITY) {
+#pragma unroll
+        for (int j = 0; j < GB; ++j) { m[j] = -INFINITY; s[j] = 0.f; acc[j] = make_float4(0.f, 0.f, 0.f, 0.f); }
+    }
+    // fold a batch into the running maxima; returns this lane's weight exp(w - m[lane % GB])
+    __device__ __forceinline__ float begin_batch(float w, int lane) {
+        const float bm = group_max<GB>(w);
+#pragma unroll
+        for (int j = 0; j < GB; ++j) {
+            const float bmj = __shfl_sync(0xffffffffu, bm, j);
+            if (bmj > m[j]) {
+                const float c = __expf(m[j] - bmj);  // m == -inf -> 0
+                acc[j].x *= c; acc[j].y *= c; acc[j].z *= c; acc[j].w *= c;
+                s[j] *= c;
+                m[j] = bmj;
+            }
         }
-        const float e = w == -INFINITY ? 0.f : __expf(w - m);
-        s += warp_sum(e);
+        m_mine = fmaxf(m_mine, bm);
+        const float e = w == -INFINITY ? 0.f : __expf(w - m_mine);
+        const float es = group_sum<GB>(e);
+#pragma unroll
+        for (int j = 0; j < GB; ++j) s[j] += __shfl_sync(0xffffffffu, es, j);
         return e;
     }
-    __device__ __forceinline__ void add(float e, float4 x) {
-        acc.x += e * x.x; acc.y += e * x.y; acc.z += e * x.z; acc.w += e * x.w;
+    __device__ __forceinline__ void add(int j, float e, float4 x) {
+        acc[j].x += e * x.x; acc[j].y += e * x.y; acc[j].z += e * x.z; acc[j].w += e * x.w;
     }
 };
 
-// One warp per output row (b, i, h); lane holds columns 4*lane .. 4*lane+3.
-// Terms: (a) the normalised partials of every CTA and pipe that covered the
-// row's unit, weighted by their lse; (b) the draft keys the tree mask lets the
-// row see (node i and its ancestors), weighted by their logits.
+// One warp per (b, i, h_kv, block of GB query heads); lane holds columns
+// 4*lane .. 4*lane+3 of the GB output rows, which are consecutive in `out` and
+// in every partial slot. Terms of each row: (b) the draft keys the tree mask
+// lets node i see (itself and its ancestors), weighted by their logits, and
+// (a) the normalised partials of every CTA and pipe that covered the unit,
+// weighted by their lse. The tree part reads nothing the cache kernel writes,
+// so it runs first and, under programmatic dependent launch, overlaps the
+// cache kernel's last CTAs; the wait for the partials comes after it. The
+// ancestor walk runs over the parent row staged in shared memory, and each
+// batch of draft K/V rows (shared by the GB heads) and of partials is loaded
+// in one go, so a warp makes a handful of round trips to memory.
+template <int GB>
 __global__ void __launch_bounds__(256) merge_tree_kernel(VerifyArgs a, SplitPlan p) {
+    extern __shared__ int32_t parent_smem[];  // [warps per block][N]
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    const int rows = a.B * a.N * a.Hq;
-    if (warp >= rows) return;
-    const int h = warp % a.Hq;
-    const int bi = warp / a.Hq;  // b * N + i
+    const int nblk = a.G / GB;
+    const int warps = a.B * a.N * a.Hkv * nblk;
+    if (warp >= warps) return;
+    const int gb = warp % nblk;
+    const int t1 = warp / nblk;
+    const int hk = t1 % a.Hkv;
+    const int bi = t1 / a.Hkv;  // b * N + i
     const int i = bi % a.N, b = bi / a.N;
-    const int hk = h / a.G, g = h - hk * a.G;
-    const int rfull = i * a.G + g;
+    const int h0 = hk * a.G + gb * GB;
+    const int64_t out_row0 = (int64_t)bi * a.Hq + h0;
+    constexpr int PER_BATCH = 32 / GB;                 // lse terms per shuffle batch
+    constexpr int TB = PER_BATCH < 8 ? PER_BATCH : 8;  // draft rows loaded per batch
+    constexpr int U = GB >= 8 ? 2 : (GB == 4 ? 4 : 8); // partial rows loaded per chunk
+    const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+
+    RowsLse<GB> st;
+    // (b) speculative part: node i and its ancestors, TB at a time
+    if (a.k_draft) {
+        int32_t *ps = parent_smem + (threadIdx.x >> 5) * a.N;
+        const int32_t *par = a.parent + (int64_t)b * a.N;
+        for (int t = lane; t <= i; t += 32) ps[t] = __ldg(par + t);
+        float4 qv[GB];
+#pragma unroll
+        for (int j = 0; j < GB; ++j) qv[j] = load_bf16x4(a.q + (out_row0 + j) * kHeadDim + 4 * lane);
+        const int64_t node_stride = (int64_t)a.Hkv * kHeadDim;
+        const __nv_bfloat16 *kd = a.k_draft + ((int64_t)b * a.N * a.Hkv + hk) * kHeadDim + 4 * lane;
+        const __nv_bfloat16 *vd = a.v_draft + ((int64_t)b * a.N * a.Hkv + hk) * kHeadDim + 4 * lane;
+        __syncwarp();
+        int j = i;
+        while (j >= 0) {
+            int mine = -1, nb = 0;
+            while (nb < TB && j >= 0) {  // lane nb records the next ancestor
+                if (lane == nb) mine = j;
+                ++nb;
+                const int pj = ps[j];
+                if (pj < -1 || pj >= j) {  // not a tree in topological order: stop here
+                    if (lane == 0) flag_status(a.status, SPEC_ERR_BAD_INPUT);
+                    j = -1;
+                } else {
+                    j = pj;
+                }
+            }
+            float4 kr[TB], vr[TB];
+#pragma unroll
+            for (int d = 0; d < TB; ++d) {
+                const int node = __shfl_sync(0xffffffffu, mine, d);
+                kr[d] = d < nb ? load_bf16x4(kd + node * node_stride) : zero4;
+                vr[d] = d < nb ? load_bf16x4(vd + node * node_stride) : zero4;
+            }
+            float logit = -INFINITY;  // lane d*GB + jj holds the logit of ancestor d for head jj
+#pragma unroll
+            for (int d = 0; d < TB; ++d) {
+                if (d < nb) {
+#pragma unroll
+                    for (int jj = 0; jj < GB; ++jj) {
+                        const float dot = warp_sum(qv[jj].x * kr[d].x + qv[jj].y * kr[d].y +
+                                                   qv[jj].z * kr[d].z + qv[jj].w * kr[d].w) * a.scale;
+                        if (lane == d * GB + jj) logit = dot;
+                    }
+                }
+            }
+            const float e = st.begin_batch(logit, lane);
+#pragma unroll
+            for (int d = 0; d < TB; ++d) {
+                if (d < nb) {
+#pragma unroll
+                    for (int jj = 0; jj < GB; ++jj) st.add(jj, __shfl_sync(0xffffffffu, e, d * GB + jj), vr[d]);
+                }
+            }
+        }
+    }
+
+    // (a) cache part: wait until the cache kernel's partials are complete and visible
+    griddep_wait();
+    const int rfull = i * a.G + gb * GB;  // first unit row of the block (a multiple of GB)
     const int rg = rfull / p.BM, ru = rfull - rg * p.BM;
     const int u = (b * a.Hkv + hk) * p.row_groups + rg;
-    // which pipe slots hold this row, and the row inside a slot
     const int h_lo = p.split_tiles ? 0 : ru / p.slot_rows;
     const int nh_shift = p.split_tiles && p.pipes == 2 ? 1 : 0;  // one or two pipe slots per CTA
     const int r = p.split_tiles ? ru : ru % p.slot_rows;
@@ -79,70 +174,48 @@ __global__ void __launch_bounds__(256) merge_tree_kernel(VerifyArgs a, SplitPlan
     const int n_parts = (c_hi - c_lo + 1) << nh_shift;
     const int64_t row0 = ((int64_t)(c_lo + u) * p.pipes + h_lo) * p.slot_rows + r;
     const int64_t cta_stride = (int64_t)p.pipes * p.slot_rows;
-
-    WarpLse st;
-    // (a) cache part
-    for (int k0 = 0; k0 < n_parts; k0 += 32) {
-        const int nb = min(32, n_parts - k0);
-        const int k = k0 + lane;
-        const float w = lane < nb ? a.lse_part[row0 + (k >> nh_shift) * cta_stride + (k & nh_shift) * p.slot_rows]
-                                  : -INFINITY;
-        const float e = st.begin_batch(w);
-#pragma unroll 4
-        for (int d = 0; d < nb; ++d) {
-            const float ed = __shfl_sync(0xffffffffu, e, d);
-            const int kd = k0 + d;
-            const int64_t row = row0 + (kd >> nh_shift) * cta_stride + (kd & nh_shift) * p.slot_rows;
-            if (ed != 0.f) st.add(ed, *reinterpret_cast<const float4 *>(a.o_part + row * kHeadDim + 4 * lane));
-        }
-    }
-    // (b) speculative part, walking node i's ancestors 32 at a time
-    if (a.k_draft) {
-        const float4 qv = load_bf16x4(a.q + (int64_t)warp * kHeadDim + 4 * lane);
-        const int32_t *par = a.parent + (int64_t)b * a.N;
-        const int64_t node_stride = (int64_t)a.Hkv * kHeadDim;
-        const __nv_bfloat16 *kd = a.k_draft + ((int64_t)b * a.N * a.Hkv + hk) * kHeadDim + 4 * lane;
-        const __nv_bfloat16 *vd = a.v_draft + ((int64_t)b * a.N * a.Hkv + hk) * kHeadDim + 4 * lane;
-        int j = i;
-        while (j >= 0) {
-            int mine = -1, nb = 0;
-            while (nb < 32 && j >= 0) {  // lane nb records the next ancestor
-                if (lane == nb) mine = j;
-                ++nb;
-                const int pj = __ldg(par + j);
-                if (pj < -1 || pj >= j) {  // not a tree in topological order: stop here
-                    if (lane == 0) flag_status(a.status, SPEC_ERR_BAD_INPUT);
-                    j = -1;
-                } else {
-                    j = pj;
+    auto part_row = [&](int k) -> int64_t {
+        return row0 + (k >> nh_shift) * cta_stride + (k & nh_shift) * p.slot_rows;
+    };
+    for (int k0 = 0; k0 < n_parts; k0 += PER_BATCH) {
+        const int nb = min(PER_BATCH, n_parts - k0);
+        const int kq = lane / GB, jq = lane & (GB - 1);
+        const float w = kq < nb ? a.lse_part[part_row(k0 + kq) + jq] : -INFINITY;
+        float e = 0.f;
+        for (int d0 = 0; d0 < nb; d0 += U) {
+            float4 x[U][GB];
+#pragma unroll
+            for (int uu = 0; uu < U; ++uu) {
+                const float *src = a.o_part + part_row(k0 + d0 + uu) * kHeadDim + 4 * lane;
+#pragma unroll
+                for (int jj = 0; jj < GB; ++jj)
+                    x[uu][jj] = d0 + uu < nb ? *reinterpret_cast<const float4 *>(src + jj * kHeadDim) : zero4;
+            }
+            if (d0 == 0) e = st.begin_batch(w, lane);  // after the first chunk's loads are issued
+#pragma unroll
+            for (int uu = 0; uu < U; ++uu) {
+                if (d0 + uu < nb) {
+#pragma unroll
+                    for (int jj = 0; jj < GB; ++jj) {
+                        const float ej = __shfl_sync(0xffffffffu, e, (d0 + uu) * GB + jj);
+                        if (ej != 0.f) st.add(jj, ej, x[uu][jj]);  // an empty partial may hold anything
+                    }
                 }
             }
-            float logit = -INFINITY;
-#pragma unroll 4
-            for (int d = 0; d < nb; ++d) {
-                const int node = __shfl_sync(0xffffffffu, mine, d);
-                const float4 kv = load_bf16x4(kd + node * node_stride);
-                const float dot = warp_sum(qv.x * kv.x + qv.y * kv.y + qv.z * kv.z + qv.w * kv.w) * a.scale;
-                if (lane == d) logit = dot;
-            }
-            const float e = st.begin_batch(logit);
-#pragma unroll 4
-            for (int d = 0; d < nb; ++d) {
-                const float ed = __shfl_sync(0xffffffffu, e, d);
-                const int node = __shfl_sync(0xffffffffu, mine, d);
-                st.add(ed, load_bf16x4(vd + node * node_stride));
-            }
         }
     }
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    float l = -INFINITY;
-    if (st.s > 0.f) {
-        const float inv = 1.f / st.s;
-        o = make_float4(st.acc.x * inv, st.acc.y * inv, st.acc.z * inv, st.acc.w * inv);
-        l = st.m + __logf(st.s);
+#pragma unroll
+    for (int j = 0; j < GB; ++j) {
+        float4 o = zero4;
+        float l = -INFINITY;
+        if (st.s[j] > 0.f) {
+            const float inv = 1.f / st.s[j];
+            o = make_float4(st.acc[j].x * inv, st.acc[j].y * inv, st.acc[j].z * inv, st.acc[j].w * inv);
+            l = st.m[j] + __logf(st.s[j]);
+        }
+        *reinterpret_cast<float4 *>(a.out + (out_row0 + j) * kHeadDim + 4 * lane) = o;
+        if (lane == 0) a.lse[out_row0 + j] = l;
     }
-    *reinterpret_cast<float4 *>(a.out + (int64_t)warp * kHeadDim + 4 * lane) = o;
-    if (lane == 0) a.lse[warp] = l;
 }
 
 // Exported two-part merge: one warp per row, any d.
@@ -177,11 +250,38 @@ __global__ void __launch_bounds__(256) lse_merge2_kernel(const float *o_a, const
 }  // namespace
 
 cudaError_t launch_merge_tree(const VerifyArgs &a, const SplitPlan &p, cudaStream_t s) {
-    const int64_t rows = (int64_t)a.B * a.N * a.Hq;
-    const int64_t blocks = (rows * 32 + 255) / 256;
-    merge_tree_kernel<<<(unsigned)blocks, 256, 0, s>>>(a, p);
+    // heads per warp: the largest of 8, 4, 2, 1 that divides G
+    const int gb = a.G % 8 == 0 ? 8 : a.G % 4 == 0 ? 4 : a.G % 2 == 0 ? 2 : 1;
+    const int64_t warps = (int64_t)a.B * a.N * a.Hkv * (a.G / gb);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((warps * 32 + 255) / 256));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = (size_t)8 * a.N * sizeof(int32_t);  // a parent row per warp
+    cfg.stream = s;
+    // programmatic dependent launch: the blocks may start while the cache kernel drains;
+    // griddepcontrol.wait inside the kernel orders the reads of its partials
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaSuccess;
+    if (cfg.dynamicSmemBytes > 48 * 1024) {  // N > 1536
+        const int smem = (int)cfg.dynamicSmemBytes;
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(merge_tree_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(merge_tree_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(merge_tree_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(merge_tree_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+    }
+    switch (gb) {
+        case 8: e = cudaLaunchKernelEx(&cfg, merge_tree_kernel<8>, a, p); break;
+        case 4: e = cudaLaunchKernelEx(&cfg, merge_tree_kernel<4>, a, p); break;
+        case 2: e = cudaLaunchKernelEx(&cfg, merge_tree_kernel<2>, a, p); break;
+        default: e = cudaLaunchKernelEx(&cfg, merge_tree_kernel<1>, a, p); break;
+    }
     count_launches(1);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_lse_merge2(const float *o_a, const float *lse_a, const float *o_b,

@@ -5,20 +5,34 @@
 // tokens by the draft-lookahead score, then the best remaining tokens by the
 // target-historical score. The result is emitted in ascending token order.
 //
-// One CTA of 1024 threads per sequence. Each tier is an exact radix select on
-// a 32-bit order-preserving key of the fp32 score (four 8-bit digit passes,
-// warp-aggregated shared-memory histograms), which yields the threshold key
-// and how many tokens equal to it are still needed; an ordered block scan
-// then gives those equal tokens to the lowest indices. The draft tier is kept
-// as a bitmap in shared memory (one bit per token), so L <= 1,572,864.
+// One thread-block cluster of 8 CTAs per sequence; CTA r owns a contiguous
+// chunk of the context, and inside it warp w owns a contiguous segment that it
+// walks 32 tokens at a time (coalesced loads, one bitmap word per step). Each
+// tier is an exact radix select on a 32-bit order-preserving key of the fp32
+// score in three digit passes (11, 11, 10 bits): every CTA histograms its
+// chunk in shared memory and adds the non-empty bins into the CTA that owns
+// them through distributed shared memory; after a cluster barrier every CTA
+// reads all totals and finds the same digit. The select yields the threshold
+// key and how many tokens equal to it are still needed; those go to the
+// lowest indices, ranked by warp ballots with CTA and warp prefixes. Tier
+// members are kept as a bitmap in shared memory (one bit per token of the
+// chunk), and the final ascending emission is one more ballot pass over it.
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace specverify {
 
 namespace {
 
-constexpr int kThreads = 1024;
+using namespace sm100;
+
+constexpr int kCtas = 8;  // CTAs per sequence (one cluster)
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
+constexpr int kBins = 2048;  // 11-bit digits
+constexpr int kSlice = kBins / kCtas;  // bins whose cluster total lives in each CTA
+constexpr int kPassesPerTier = 3;
+static_assert(kBins == 4 * kThreads, "four bins per thread in the digit search");
 
 // Order-preserving key: larger score -> larger key; -0 == +0; NaN -> 0, below
 // every number (the smallest key of a number, -inf, is 0x007fffff).
@@ -29,11 +43,51 @@ __device__ __forceinline__ uint32_t order_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// digit of pass p: key bits [31..21], [20..10], [9..0]
+__device__ __forceinline__ int pass_shift(int p) { return p == 0 ? 21 : (p == 1 ? 10 : 0); }
+__device__ __forceinline__ uint32_t pass_hi_mask(int p) { return p == 0 ? 0u : (p == 1 ? 0xffe00000u : 0xfffffc00u); }
+__device__ __forceinline__ uint32_t pass_digit_mask(int p) { return p == 2 ? 0x3ffu : 0x7ffu; }
+
 struct SelectSmem {
-    uint32_t hist[256];
+    uint32_t hist[kBins];                      // this CTA's histogram of the current pass
+    uint32_t acc[2 * kPassesPerTier][kSlice];  // cluster totals of the owned bins, one buffer per pass
+    uint32_t xcnt[3][kCtas];                   // per-CTA counts, written by every CTA of the cluster
     uint32_t warp_tot[kWarps];
     uint32_t bcast[4];
 };
+
+// Tokens per CTA for a context of n: ceil(n / kCtas) rounded up to a multiple
+// of 4 * kThreads, so every warp walks a multiple of four 32-token rounds.
+__host__ __device__ __forceinline__ int chunk_tokens(int n) {
+    return ((n + kCtas - 1) / kCtas + 4 * kThreads - 1) / (4 * kThreads) * (4 * kThreads);
+}
+
+// The chunk of one CTA: tokens [base, base + C) of the context [0, n), warp w
+// owning [seg0, seg0 + 32 * rounds).
+struct Chunk {
+    int n, lo, hi;  // context length and the candidate range [lo, hi) (outside sink and window)
+    int seg0, rounds;  // rounds: a multiple of 4
+};
+
+// Keys of rounds kk0 .. kk0+3 of this lane: from the warp's staged copy in
+// shared memory, or straight from the scores (four loads in flight).
+template <bool STAGED>
+__device__ __forceinline__ void fetch4(uint32_t (&key)[4], const float *score, const uint32_t *staged,
+                                       const Chunk &c, int kk0, int lane) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int kk = kk0 + u;
+        const int t = c.seg0 + kk * 32 + lane;
+        if (STAGED) key[u] = staged[kk * 32 + lane];
+        else key[u] = t < c.n ? order_key(__ldg(score + t)) : 0u;
+    }
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
 
 // Exclusive block scan of one value per thread; returns the prefix, *total = sum.
 __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, SelectSmem &sm, uint32_t *total) {
@@ -41,20 +95,20 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, SelectSmem 
     uint32_t x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
     }
     if (lane == 31) sm.warp_tot[wid] = x;
     __syncthreads();
     if (wid == 0) {
-        uint32_t t = sm.warp_tot[lane];
+        const uint32_t t = lane < kWarps ? sm.warp_tot[lane] : 0u;
         uint32_t s = t;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            uint32_t y = __shfl_up_sync(0xffffffffu, s, o);
+            const uint32_t y = __shfl_up_sync(0xffffffffu, s, o);
             if (lane >= o) s += y;
         }
-        sm.warp_tot[lane] = s - t;  // exclusive prefix of the warp totals
+        if (lane < kWarps) sm.warp_tot[lane] = s - t;  // exclusive prefix of the warp totals
         if (lane == 31) sm.bcast[0] = s;
     }
     __syncthreads();
@@ -64,60 +118,95 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, SelectSmem 
     return r;
 }
 
-__device__ __forceinline__ bool bit_set(const uint32_t *bits, int t) {
-    return (bits[t >> 5] >> (t & 31)) & 1u;
+// Warp-uniform count per warp -> the sum over the warps before this one; *total = CTA sum.
+__device__ __forceinline__ uint32_t warp_prefix(uint32_t wcount, SelectSmem &sm, uint32_t *total) {
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) sm.warp_tot[warp] = wcount;
+    __syncthreads();
+    uint32_t before = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const uint32_t x = sm.warp_tot[w];
+        all += x;
+        before += w < warp ? x : 0u;
+    }
+    __syncthreads();
+    *total = all;
+    return before;
 }
 
-// k-th largest key (k >= 1) among tokens t in [lo, hi) not in `exclude`.
-// Returns the key; *need = how many tokens with exactly that key belong to the top k.
-__device__ uint32_t radix_select(const float *score, int lo, int hi, const uint32_t *exclude,
-                                 uint32_t k, SelectSmem &sm, uint32_t *need) {
-    uint32_t prefix = 0u;
-    uint32_t kr = k;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = threadIdx.x; i < 256; i += kThreads) sm.hist[i] = 0u;
+// CTA-uniform value v of every CTA of the cluster -> the sum over the CTAs
+// before this one; *total = cluster sum. One cluster barrier.
+__device__ __forceinline__ uint32_t cluster_exchange(uint32_t v, int ph, uint32_t rank, SelectSmem &sm,
+                                                     uint32_t *total) {
+    if (threadIdx.x < kCtas) dsmem_st(dsmem_map(&sm.xcnt[ph][rank], threadIdx.x), v);
+    cluster_sync();
+    uint32_t before = 0, all = 0;
+#pragma unroll
+    for (int q = 0; q < kCtas; ++q) {
+        const uint32_t x = sm.xcnt[ph][q];
+        all += x;
+        before += q < (int)rank ? x : 0u;
+    }
+    *total = all;
+    return before;
+}
+
+__device__ __forceinline__ bool candidate(const Chunk &c, int t, const uint32_t *excl, int word, int lane) {
+    return t >= c.lo && t < c.hi && !(excl && ((excl[word] >> lane) & 1u));
+}
+
+// k-th largest key (1 <= k <= candidates) among the candidates of the whole
+// sequence not marked in `excl`. Returns the key; *need = how many tokens with
+// exactly that key belong to the top k. Every CTA of the cluster returns the
+// same values. Uses acc buffers buf .. buf + 2.
+template <bool STAGED>
+__device__ uint32_t cluster_select(const float *score, const uint32_t *staged, const Chunk &c,
+                                   const uint32_t *excl, uint32_t k, SelectSmem &sm, int buf, uint32_t *need) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t prefix = 0u, kr = k;
+    for (int p = 0; p < kPassesPerTier; ++p) {
+        const int shift = pass_shift(p);
+        const uint32_t him = pass_hi_mask(p), dm = pass_digit_mask(p);
+        for (int i = tid; i < kBins; i += kThreads) sm.hist[i] = 0u;
         __syncthreads();
-        const uint32_t hi_mask = shift == 24 ? 0u : (0xffffffffu << (shift + 8));
-        for (int base = lo; base < hi; base += kThreads) {
-            const int t = base + threadIdx.x;
-            int digit = -1;
-            if (t < hi && !(exclude && bit_set(exclude, t))) {
-                const uint32_t key = order_key(__ldg(score + t));
-                if ((key & hi_mask) == (prefix & hi_mask)) digit = (key >> shift) & 0xffu;
+        for (int kk0 = 0; kk0 < c.rounds; kk0 += 4) {
+            uint32_t key[4];
+            fetch4<STAGED>(key, score, staged, c, kk0, lane);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int t = c.seg0 + (kk0 + u) * 32 + lane;
+                if (candidate(c, t, excl, warp * c.rounds + kk0 + u, lane) && (key[u] & him) == (prefix & him))
+                    atomicAdd(&sm.hist[(key[u] >> shift) & dm], 1u);
             }
-            // one shared atomic per distinct digit in the warp
-            const unsigned peers = __match_any_sync(0xffffffffu, digit);
-            const int leader = __ffs(peers) - 1;
-            if (digit >= 0 && (threadIdx.x & 31) == leader) atomicAdd(&sm.hist[digit], __popc(peers));
         }
         __syncthreads();
-        if (threadIdx.x < 32) {
-            // lane l owns digits 255-8l .. 248-8l (descending order of digits)
-            const int lane = threadIdx.x;
-            uint32_t own = 0;
+        uint32_t *acc = sm.acc[buf + p];
+        for (int i = tid; i < kBins; i += kThreads) {
+            const uint32_t v = sm.hist[i];
+            if (v) dsmem_red_add(dsmem_map(&acc[i % kSlice], i / kSlice), v);
+        }
+        cluster_sync();
+        // cluster totals, four bins per thread in descending digit order
+        uint32_t cnt[4], own = 0;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) own += sm.hist[255 - 8 * lane - j];
-            uint32_t incl = own;
+        for (int j = 0; j < 4; ++j) {
+            const int d = kBins - 1 - (4 * tid + j);
+            cnt[j] = dsmem_ld(dsmem_map(&acc[d % kSlice], d / kSlice));
+            own += cnt[j];
+        }
+        uint32_t total;
+        const uint32_t before = block_exclusive_scan(own, sm, &total);
+        if (before < kr && before + own >= kr) {  // exactly one thread
+            uint32_t cum = before;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            const uint32_t excl = incl - own;
-            const unsigned hit = __ballot_sync(0xffffffffu, excl < kr && incl >= kr);
-            const int owner = __ffs(hit) - 1;  // exactly one lane when kr <= candidates
-            if (lane == owner) {
-                uint32_t cum = excl;
-                for (int j = 0; j < 8; ++j) {
-                    const int dgt = 255 - 8 * lane - j;
-                    const uint32_t c = sm.hist[dgt];
-                    if (cum + c >= kr) {
-                        sm.bcast[1] = (uint32_t)dgt;
-                        sm.bcast[2] = kr - cum;
-                        break;
-                    }
-                    cum += c;
+            for (int j = 0; j < 4; ++j) {
+                if (cum + cnt[j] >= kr) {
+                    sm.bcast[1] = (uint32_t)(kBins - 1 - (4 * tid + j));
+                    sm.bcast[2] = kr - cum;
+                    break;
                 }
+                cum += cnt[j];
             }
         }
         __syncthreads();
@@ -129,136 +218,144 @@ __device__ uint32_t radix_select(const float *score, int lo, int hi, const uint3
     return prefix;
 }
 
-// Marks into `out_bits` (words owned per thread) the top-k of [lo, hi) \ exclude:
-// keys above `thr`, plus the first `need` tokens (by index) whose key equals `thr`.
-__device__ void mark_tier(const float *score, int lo, int hi, const uint32_t *exclude,
-                          uint32_t thr, uint32_t need, uint32_t *out_bits, int w0, int w1,
-                          SelectSmem &sm) {
-    uint32_t eq = 0;
-    for (int w = w0; w < w1; ++w) {
-        for (int j = 0; j < 32; ++j) {
-            const int t = w * 32 + j;
-            if (t < lo || t >= hi || (exclude && bit_set(exclude, t))) continue;
-            eq += order_key(__ldg(score + t)) == thr;
+// ORs into `bits` the top-k of the candidates not already in `excl`: keys
+// above `thr`, plus the first `need` tokens (by index, over the whole
+// sequence) whose key equals `thr`. `excl` may alias `bits`: each warp reads
+// and writes only its own words, a word's read before its write.
+template <bool STAGED>
+__device__ void mark_tier(const float *score, const uint32_t *staged, const Chunk &c, const uint32_t *excl,
+                          uint32_t *bits, uint32_t thr, uint32_t need, int ph, uint32_t rank, SelectSmem &sm) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t weq = 0;
+    for (int kk0 = 0; kk0 < c.rounds; kk0 += 4) {
+        uint32_t key[4];
+        fetch4<STAGED>(key, score, staged, c, kk0, lane);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int t = c.seg0 + (kk0 + u) * 32 + lane;
+            const bool eq = candidate(c, t, excl, warp * c.rounds + kk0 + u, lane) && key[u] == thr;
+            weq += __popc(__ballot_sync(0xffffffffu, eq));
         }
     }
-    uint32_t total;
-    uint32_t rank = block_exclusive_scan(eq, sm, &total);
-    for (int w = w0; w < w1; ++w) {
-        uint32_t word = 0;
-        for (int j = 0; j < 32; ++j) {
-            const int t = w * 32 + j;
-            if (t < lo || t >= hi || (exclude && bit_set(exclude, t))) continue;
-            const uint32_t key = order_key(__ldg(score + t));
-            bool take = key > thr;
-            if (key == thr) {
-                take = rank < need;
-                ++rank;
-            }
-            word |= (uint32_t)take << j;
+    uint32_t cta_eq, eq_all;
+    const uint32_t warp_before = warp_prefix(weq, sm, &cta_eq);
+    const uint32_t cta_before = cluster_exchange(cta_eq, ph, rank, sm, &eq_all);
+    const bool all_eq = need >= eq_all;
+    uint32_t run = cta_before + warp_before;  // rank of this warp's next equal key
+    for (int kk0 = 0; kk0 < c.rounds; kk0 += 4) {
+        uint32_t key[4];
+        fetch4<STAGED>(key, score, staged, c, kk0, lane);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int t = c.seg0 + (kk0 + u) * 32 + lane;
+            const int word = warp * c.rounds + kk0 + u;
+            const bool cand = candidate(c, t, excl, word, lane);
+            const bool eq = cand && key[u] == thr;
+            const unsigned eqm = __ballot_sync(0xffffffffu, eq);
+            const bool take = cand && (key[u] > thr || (eq && (all_eq || run + __popc(eqm & lanemask_lt()) < need)));
+            const unsigned w = __ballot_sync(0xffffffffu, take);
+            if (lane == 0) bits[word] |= w;
+            run += __popc(eqm);
         }
-        out_bits[w] = word;
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-select_topk_kernel(const float *__restrict__ draft, const float *__restrict__ target, int64_t ld,
-                   int L, const int32_t *__restrict__ ctx_lens, int sink, int window, int top_m,
-                   int budget, int32_t *__restrict__ idx, int32_t *__restrict__ count,
-                   uint32_t *status) {
+// Copies this warp's keys of `score` into its staged segment.
+__device__ __forceinline__ void stage_keys(const float *score, uint32_t *staged, const Chunk &c, int lane) {
+    for (int kk0 = 0; kk0 < c.rounds; kk0 += 4) {
+        uint32_t key[4];
+        fetch4<false>(key, score, nullptr, c, kk0, lane);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) staged[(kk0 + u) * 32 + lane] = key[u];
+    }
+    __syncwarp();
+}
+
+template <bool STAGED>
+__global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
+select_topk_kernel(const float *__restrict__ draft, const float *__restrict__ target, int64_t ld, int L,
+                   const int32_t *__restrict__ ctx_lens, int sink, int window, int top_m, int budget,
+                   int32_t *__restrict__ idx, int32_t *__restrict__ count, uint32_t *status) {
     extern __shared__ __align__(16) uint32_t dyn[];
-    __shared__ SelectSmem sm;
-    const int b = blockIdx.x;
+    SelectSmem &sm = *reinterpret_cast<SelectSmem *>(dyn);
+    uint32_t *bits = dyn + sizeof(SelectSmem) / sizeof(uint32_t);  // [C / 32] tier membership
+    const uint32_t rank = cluster_ctarank();
+    const int b = blockIdx.x / kCtas;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int n = L;
     if (ctx_lens) {
         n = ctx_lens[b];
         if (n < 0 || n > L) {
-            if (threadIdx.x == 0) flag_status(status, SPEC_ERR_BAD_INPUT);
+            if (rank == 0 && tid == 0) flag_status(status, SPEC_ERR_BAD_INPUT);
             n = n < 0 ? 0 : L;
         }
     }
     int32_t *out = idx + (int64_t)b * budget;
-    if (budget >= n) {  // the whole context fits: verify in full
-        for (int j = threadIdx.x; j < budget; j += kThreads) out[j] = j < n ? j : -1;
-        if (count && threadIdx.x == 0) count[b] = n;
+    if (budget >= n) {  // the whole context fits: verify in full (uniform over the cluster)
+        for (int j = (int)rank * kThreads + tid; j < budget; j += kCtas * kThreads) out[j] = j < n ? j : -1;
+        if (count && rank == 0 && tid == 0) count[b] = n;
         return;
     }
     const float *ds = draft + (int64_t)b * ld;
     const float *ts = target + (int64_t)b * ld;
     const int s0 = sink < n ? sink : n;
     const int w0n = window < n - s0 ? window : n - s0;
-    const int lo = s0, hi = n - w0n;
-    int left = budget - s0 - w0n;
+    Chunk c;
+    c.n = n;
+    c.lo = s0;
+    c.hi = n - w0n;
+    const int left = budget - s0 - w0n;
     int m = top_m < left ? top_m : left;
-    if (m > hi - lo) m = hi - lo;
+    if (m > c.hi - c.lo) m = c.hi - c.lo;
     const int f = left - m;
+    const int C = chunk_tokens(n);
+    c.rounds = C / kThreads;
+    c.seg0 = (int)rank * C + warp * c.rounds * 32;
+    const int nwords = kWarps * c.rounds;
+    // staged keys: [C] after the bitmap, warp w's segment at w * 32 * rounds
+    uint32_t *staged = bits + chunk_tokens(L) / 32 + warp * c.rounds * 32;
 
-    const int nwords = (n + 31) >> 5;
-    const int wpt = (nwords + kThreads - 1) / kThreads;
-    const int wa = threadIdx.x * wpt;
-    const int wb = min(wa + wpt, nwords);
-    uint32_t *dbits = dyn;  // [nwords] draft-tier membership
+    for (int i = tid; i < 2 * kPassesPerTier * kSlice; i += kThreads) (&sm.acc[0][0])[i] = 0u;
+    for (int i = tid; i < nwords; i += kThreads) bits[i] = 0u;
+    cluster_sync();  // peers are running and their totals are zero before any remote add
 
-    // tier 1: top-m by draft score
-    if (m > 0) {
+    int buf = 0;
+    if (m > 0) {  // tier 1: top-m by draft score
+        if (STAGED) stage_keys(ds, staged, c, lane);
         uint32_t need;
-        const uint32_t thr = radix_select(ds, lo, hi, nullptr, (uint32_t)m, sm, &need);
-        mark_tier(ds, lo, hi, nullptr, thr, need, dbits, wa, wb, sm);
-    } else {
-        for (int w = wa; w < wb; ++w) dbits[w] = 0u;
+        const uint32_t thr = cluster_select<STAGED>(ds, staged, c, nullptr, (uint32_t)m, sm, buf, &need);
+        buf += kPassesPerTier;
+        mark_tier<STAGED>(ds, staged, c, nullptr, bits, thr, need, 0, rank, sm);
+        __syncthreads();
     }
-    __syncthreads();
-    // tier 2: fill by target score among the rest; reuse each thread's own words
-    uint32_t thr_f = 0, need_f = 0;
-    if (f > 0) thr_f = radix_select(ts, lo, hi, dbits, (uint32_t)f, sm, &need_f);
-    // final ordered pass: selected = sink u window u D u F, emitted ascending
-    uint32_t eq = 0;
-    if (f > 0) {
-        for (int w = wa; w < wb; ++w)
-            for (int j = 0; j < 32; ++j) {
-                const int t = w * 32 + j;
-                if (t < lo || t >= hi || bit_set(dbits, t)) continue;
-                eq += order_key(__ldg(ts + t)) == thr_f;
-            }
+    if (f > 0) {  // tier 2: fill by target score among the rest
+        if (STAGED) stage_keys(ts, staged, c, lane);
+        uint32_t need;
+        const uint32_t thr = cluster_select<STAGED>(ts, staged, c, bits, (uint32_t)f, sm, buf, &need);
+        mark_tier<STAGED>(ts, staged, c, bits, bits, thr, need, 1, rank, sm);
+        __syncthreads();
     }
-    uint32_t eq_total;
-    uint32_t eq_rank = block_exclusive_scan(eq, sm, &eq_total);
-    // count selected per thread, in index order
-    uint32_t sel = 0;
-    uint32_t r2 = eq_rank;
-    for (int w = wa; w < wb; ++w)
-        for (int j = 0; j < 32; ++j) {
-            const int t = w * 32 + j;
-            if (t >= n) continue;
-            bool take;
-            if (t < lo || t >= hi) take = true;
-            else if (bit_set(dbits, t)) take = true;
-            else if (f > 0) {
-                const uint32_t key = order_key(__ldg(ts + t));
-                take = key > thr_f;
-                if (key == thr_f) { take = r2 < need_f; ++r2; }
-            } else take = false;
-            sel += take;
-        }
-    uint32_t total;
-    uint32_t pos = block_exclusive_scan(sel, sm, &total);
-    r2 = eq_rank;
-    for (int w = wa; w < wb; ++w)
-        for (int j = 0; j < 32; ++j) {
-            const int t = w * 32 + j;
-            if (t >= n) continue;
-            bool take;
-            if (t < lo || t >= hi) take = true;
-            else if (bit_set(dbits, t)) take = true;
-            else if (f > 0) {
-                const uint32_t key = order_key(__ldg(ts + t));
-                take = key > thr_f;
-                if (key == thr_f) { take = r2 < need_f; ++r2; }
-            } else take = false;
-            if (take && pos < (uint32_t)budget) out[pos++] = t;
-        }
-    for (int j = (int)total + threadIdx.x; j < budget; j += kThreads) out[j] = -1;
-    if (count && threadIdx.x == 0) count[b] = (int32_t)(total < (uint32_t)budget ? total : budget);
+    // emission: sink u window u tiers, ascending
+    uint32_t wsel = 0;
+    for (int kk = 0; kk < c.rounds; ++kk) {
+        const int t = c.seg0 + kk * 32 + lane;
+        const bool sel = t < n && (t < c.lo || t >= c.hi || ((bits[warp * c.rounds + kk] >> lane) & 1u));
+        wsel += __popc(__ballot_sync(0xffffffffu, sel));
+    }
+    uint32_t cta_sel, all_sel;
+    const uint32_t warp_before = warp_prefix(wsel, sm, &cta_sel);
+    const uint32_t cta_before = cluster_exchange(cta_sel, 2, rank, sm, &all_sel);
+    uint32_t pos = cta_before + warp_before;
+    for (int kk = 0; kk < c.rounds; ++kk) {
+        const int t = c.seg0 + kk * 32 + lane;
+        const bool sel = t < n && (t < c.lo || t >= c.hi || ((bits[warp * c.rounds + kk] >> lane) & 1u));
+        const unsigned msk = __ballot_sync(0xffffffffu, sel);
+        const uint32_t p = pos + __popc(msk & lanemask_lt());
+        if (sel && p < (uint32_t)budget) out[p] = t;
+        pos += __popc(msk);
+    }
+    for (int j = (int)all_sel + (int)rank * kThreads + tid; j < budget; j += kCtas * kThreads) out[j] = -1;
+    if (count && rank == 0 && tid == 0) count[b] = (int32_t)(all_sel < (uint32_t)budget ? all_sel : budget);
 }
 
 }  // namespace
@@ -268,12 +365,19 @@ cudaError_t launch_select_topk(const float *ds, const float *ts, int64_t ld, int
                                int budget, int32_t *idx, int32_t *count, uint32_t *status,
                                cudaStream_t s) {
     if (B == 0) return cudaSuccess;
-    const size_t smem = (size_t)((L + 31) / 32) * sizeof(uint32_t);
-    cudaError_t e = cudaFuncSetAttribute(select_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    select_topk_kernel<<<B, kThreads, smem, s>>>(ds, ts, ld, L, ctx_lens, sink, window, top_m, budget,
-                                                 idx, count, status);
+    const size_t C = (size_t)chunk_tokens(L);
+    const size_t base = sizeof(SelectSmem) + C / 32 * sizeof(uint32_t);
+    const size_t staged = base + C * sizeof(uint32_t);
+    // keys staged in shared memory while the chunk fits (L up to about 360k), else read from L2 each pass
+    const bool use_staged = staged <= 200 * 1024;
+    const size_t smem = use_staged ? staged : base;
+    auto kern = use_staged ? select_topk_kernel<true> : select_topk_kernel<false>;
+    if (smem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    kern<<<(unsigned)B * kCtas, kThreads, smem, s>>>(ds, ts, ld, L, ctx_lens, sink, window, top_m, budget, idx,
+                                                     count, status);
     count_launches(1);
     return cudaGetLastError();
 }
