@@ -118,11 +118,11 @@ spec_status_t verify_common(const uint16_t *q, const uint16_t *k_cache, const ui
     if (cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s) != cudaSuccess) return SPEC_ERR_CUDA;
     cudaEvent_t ev0 = g_prof_start && g_prof_stop ? g_prof_start : nullptr;
     cudaEvent_t ev1 = ev0 ? g_prof_stop : nullptr;
-    // dense: the tensor-core (tcgen05/TMA) kernel when the shape allows its TMA maps;
-    // sparse and the other shapes: the warp-level tensor-core kernel
+    // the tcgen05 kernel when the shape allows it (its TMA maps, its 16-byte row gathers);
+    // the other shapes: the warp-level tensor-core kernel
     SplitPlan plan;
     bool launched = false;
-    if (!sparse && tc_supported(a)) {
+    if (tc_supported(a)) {
         plan = make_plan_tc(B, N, Hq, Hkv, L_eff, dev.sms);
         a.o_part = reinterpret_cast<float *>(ws + kHeaderBytes);
         a.lse_part = reinterpret_cast<float *>(ws + kHeaderBytes + plan_o_bytes(plan, d));

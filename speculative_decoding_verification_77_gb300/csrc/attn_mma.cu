@@ -74,12 +74,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 template <bool SPARSE>
 __device__ __forceinline__ int cache_token(const VerifyArgs &a, int b, int n, int p, bool report) {
     if (!SPARSE) return p < n ? p : -1;
-    if (p >= a.budget) return -1;
-    const int32_t *ib = a.idx + (int64_t)b * a.budget;
-    const int t = __ldg(ib + p);
-    const bool ok = t >= 0 && t < n && (p == 0 || t > __ldg(ib + p - 1));
-    if (!ok && t != -1 && report) flag_status(a.status, SPEC_ERR_BAD_INPUT);
-    return ok ? t : -1;
+    return sparse_token(a, b, n, p, report);
 }
 
 template <bool SPARSE>

@@ -1,5 +1,6 @@
 // Cache part of verification attention on the 5th-generation tensor core
-// (tcgen05 + TMEM + TMA), for the dense full-cache case.
+// (tcgen05 + TMEM + TMA), for the full cache (dense) and for the selected
+// index set (sparse).
 //
 // What it computes is the same normalised split-KV partial as the warp-level
 // kernel: for every unit (b, h_kv, group of query rows: the query heads of
@@ -8,11 +9,23 @@
 // that range, with no mask but "token < n" (the cache part needs none, LongSpec
 // section 2.C). Partials are merged by log-sum-exp with the tree part later.
 //
+// Sparse (Dustin, "Workflow di Verifica"): tile t holds index slots
+// [128 t, 128 t + 128) of idx[b]; a slot whose entry is unused (padding, out of
+// the context, not ascending) is a zero row in shared memory and a masked
+// column of S.
+//
 // Design (one CTA per SM, persistent over its balanced range of tiles):
-//   warp 8      TMA producer: the unit's Q rows (3-D map over [B*N, Hq, d], so
-//               query heads x draft nodes land as consecutive rows), then a
-//               5-slot ring of K and V tiles (4-D map over [B, Hkv, L, d] with
-//               the caller's strides), 128-byte swizzle.
+//   warp 8      producer: the unit's Q rows by TMA (3-D map over [B*N, Hq, d],
+//               so query heads x draft nodes land as consecutive rows), then a
+//               5-slot ring of K and V tiles, 128-byte swizzle. Dense: TMA
+//               (4-D map over [B, Hkv, L, d] with the caller's strides). Sparse:
+//               the whole warp gathers the rows with 16-byte cp.async into the
+//               same swizzled layout, two rows of 256 bytes per instruction;
+//               every lane then arms an arrival on the slot's barrier that fires
+//               when its copies have landed (32 arrivals complete the slot), so
+//               the producer never waits for its own copies. The MMA warp fences
+//               the async proxy after the wait, before the tensor core reads the
+//               slot.
 //   warp 9      MMA issuer (one thread): S_h = Q_h K^T (A and B from shared
 //               memory) and O_h += P_h V (P from TMEM, V MN-major from shared
 //               memory), fp32 accumulators in TMEM, tcgen05.commit to mbarriers.
@@ -117,6 +130,7 @@ __device__ __forceinline__ int seg_tile(const Seg &s, int split_tiles, int h, in
     return split_tiles ? s.tb + 2 * i + h : s.tb + i;
 }
 
+template <bool SPARSE>
 __global__ void __launch_bounds__(THREADS, 1)
 cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
                      const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -136,7 +150,7 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
         mbar_init(&bs.q_full, 1);
         mbar_init(&bs.q_empty, 1);
         for (int i = 0; i < RING; ++i) {
-            mbar_init(&bs.kv_full[i], 1);
+            mbar_init(&bs.kv_full[i], SPARSE ? 32 : 1);  // sparse: one arrival per gathering lane
             mbar_init(&bs.kv_empty[i], 1);
         }
         for (int h = 0; h < 2; ++h) {
@@ -161,7 +175,77 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
     const int64_t g0 = plan_start(p, blockIdx.x), g1 = plan_start(p, blockIdx.x + 1);
     const int64_t u_first = g0 / p.tiles_per_unit;
 
-    if (warp == WARP_PRODUCER) {
+    if (SPARSE && warp == WARP_PRODUCER) {
+        // ------------------------------------------------------------ gather producer
+        if (lane == 0) tma_prefetch_desc(&tm_q);
+        int64_t item = 0;  // K/V tiles issued (same in all lanes)
+        int seg_i = 0, q_loads = 0;
+        bool ok = true;
+        // Copy pattern: in step v (0..31), lane l copies 16-byte chunk c = l & 7 of both
+        // 128-byte halves of tile row r = 4v + (l >> 3): every instruction moves four whole
+        // 128-byte lines. Row r lands at r * 128 bytes of each half, its chunks permuted by
+        // the 128-byte swizzle (c ^ (r & 7), and r & 7 = 4 (v & 1) + (l >> 3)).
+        const int rs = lane >> 3, c8 = lane & 7;
+        const uint32_t xo0 = (uint32_t)((c8 ^ rs) << 4), xo1 = (uint32_t)((c8 ^ (4 + rs)) << 4);
+        const int64_t row_bytes = a.st * 2;
+        for (int64_t u = u_first; ok && u * p.tiles_per_unit < g1; ++u, ++seg_i) {
+            Seg s;
+            seg_decode(a, p, split_tiles, u, g0, g1, s);
+            if (seg_i > 0 && !(ok = __all_sync(0xffffffffu, wait_bar(bs, &bs.q_empty, (seg_i - 1) & 1, a.status))))
+                break;
+            if (lane == 0) {
+                const int npipe_q = split_tiles ? 1 : 2;
+                mbar_arrive_expect_tx(&bs.q_full, npipe_q * 2 * 16384);
+                for (int h = 0; h < npipe_q; ++h) {
+                    const int n0 = (s.rg * BM + 128 * h) / a.G;
+                    for (int kh = 0; kh < 2; ++kh)
+                        tma_load_3d(sQ + kh * 32768 + h * 16384, &tm_q, &bs.q_full, kh * 64, s.hk * a.G,
+                                    s.b * a.N + n0);
+                }
+            }
+            ++q_loads;
+            const int n_ctx = context_len(a, s.b);
+            const char *kbase = reinterpret_cast<const char *>(a.k_cache + s.b * a.sb + s.hk * a.sh);
+            const char *vbase = reinterpret_cast<const char *>(a.v_cache + s.b * a.sb + s.hk * a.sh);
+            IdxPair raw[4];  // index entries of the next tile, loaded one tile ahead
+#pragma unroll
+            for (int u4 = 0; u4 < 4; ++u4) raw[u4] = sparse_raw(a, s.b, s.tb * T + 32 * u4 + lane);
+            for (int t = s.tb; ok && t < s.te; ++t) {
+                int tok[4];  // token of index slot 128 t + 32 u + lane, or -1
+#pragma unroll
+                for (int u4 = 0; u4 < 4; ++u4) tok[u4] = sparse_resolve(a, raw[u4], t * T + 32 * u4 + lane, n_ctx, true);
+                if (t + 1 < s.te) {
+#pragma unroll
+                    for (int u4 = 0; u4 < 4; ++u4) raw[u4] = sparse_raw(a, s.b, (t + 1) * T + 32 * u4 + lane);
+                }
+                int tkr[32];  // token of tile row 4v + rs, or -1
+#pragma unroll
+                for (int v = 0; v < 32; ++v) tkr[v] = __shfl_sync(0xffffffffu, tok[v >> 3], (4 * v + rs) & 31);
+                for (int kv = 0; kv < 2; ++kv) {
+                    const int slot = (int)(item % RING);
+                    const int64_t use = item / RING;
+                    if (use > 0 &&
+                        !(ok = __all_sync(0xffffffffu, wait_bar(bs, &bs.kv_empty[slot], (uint32_t)((use - 1) & 1), a.status))))
+                        break;
+                    const char *base = (kv ? vbase : kbase) + c8 * 16;
+                    const uint32_t d0 = smem_u32(sRing + slot * SLOT_BYTES) + (uint32_t)rs * 128u;
+#pragma unroll
+                    for (int v = 0; v < 32; ++v) {
+                        const bool ok_row = tkr[v] >= 0;
+                        const char *src = ok_row ? base + (int64_t)tkr[v] * row_bytes : reinterpret_cast<const char *>(a.q);
+                        const uint32_t d = d0 + (uint32_t)v * 512u + ((v & 1) ? xo1 : xo0);
+                        cp_async16_zfill(d, src, ok_row);                    // columns 0-63
+                        cp_async16_zfill(d + HALF_BYTES, src + 128, ok_row);  // columns 64-127
+                    }
+                    cp_async_mbar_arrive_noinc(&bs.kv_full[slot]);
+                    ++item;
+                }
+            }
+        }
+        cp_async_wait_all();  // the drain: no copy is left in flight
+        if (lane == 0 && q_loads > 0) drain_wait(&bs.q_full, (q_loads - 1) & 1);
+        __syncwarp();
+    } else if (warp == WARP_PRODUCER) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
@@ -235,6 +319,7 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
                     // pipe 1 of a shared tile reuses the K tile pipe 0 already waited for
                     if ((split_tiles || h == 0) && !__all_sync(0xffffffffu, wait_bar(bs, &bs.kv_full[slot], (n / RING) & 1u, a.status)))
                         return false;
+                    if (SPARSE) fence_proxy_async_smem();  // the slot was written by cp.async (generic proxy)
                     const uint64_t dq = h ? dq1 : dq0;
                     const uint64_t dk = dk0 + (uint64_t)slot * (SLOT_BYTES >> 4);
                     const uint32_t d_tmem = tmem + 128u * h;
@@ -256,6 +341,7 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
                     const uint32_t slot = n % RING;
                     if ((split_tiles || h == 0) && !__all_sync(0xffffffffu, wait_bar(bs, &bs.kv_full[slot], (n / RING) & 1u, a.status)))
                         return false;
+                    if (SPARSE) fence_proxy_async_smem();  // the slot was written by cp.async (generic proxy)
                     tc_fence_after();  // P_h was written to TMEM by the softmax warps
                     const uint64_t dv = dv0 + (uint64_t)slot * (SLOT_BYTES >> 4);
                     const uint32_t d_tmem = tmem + 256u + 128u * h, a_tmem = tmem + 128u * h;
@@ -313,8 +399,26 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
             }
             const int n_ctx = context_len(a, s.b);
             float m_ref = -INFINITY, l = 0.f;
+            IdxPair raw[4];  // sparse: index entries of this pipe's next tile, loaded one tile ahead
+            if (SPARSE && warp_rows) {
+                const int t0 = seg_tile(s, split_tiles, h, 0);
+#pragma unroll
+                for (int u4 = 0; u4 < 4; ++u4) raw[u4] = sparse_raw(a, s.b, t0 * T + 32 * u4 + lane);
+            }
             for (int k = 0; k < s.cnt[h]; ++k) {
                 const int t = seg_tile(s, split_tiles, h, k);
+                uint32_t vmask[4] = {~0u, ~0u, ~0u, ~0u};  // sparse: used index slots of the tile
+                if (SPARSE && warp_rows) {
+#pragma unroll
+                    for (int u4 = 0; u4 < 4; ++u4)
+                        vmask[u4] = __ballot_sync(0xffffffffu,
+                                                  sparse_resolve(a, raw[u4], t * T + 32 * u4 + lane, n_ctx, false) >= 0);
+                    if (k + 1 < s.cnt[h]) {
+                        const int tn = seg_tile(s, split_tiles, h, k + 1);
+#pragma unroll
+                        for (int u4 = 0; u4 < 4; ++u4) raw[u4] = sparse_raw(a, s.b, tn * T + 32 * u4 + lane);
+                    }
+                }
                 ok = __all_sync(0xffffffffu, ok && wait_bar(bs, &bs.s_full[h], s_count & 1, a.status));
                 ++s_count;
                 tc_fence_after();
@@ -323,13 +427,23 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
 #pragma unroll
                     for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_addr + s_col + 32u * c, r[c]);
                     tmem_wait_ld();
-                    const int valid = min(max(n_ctx - t * T, 0), T);  // tokens of this tile inside the context
-                    if (valid < T) {  // tail tile (warp-uniform): mask the tokens past the context
+                    if (SPARSE) {
+                        if ((vmask[0] & vmask[1] & vmask[2] & vmask[3]) != ~0u) {  // warp-uniform
 #pragma unroll
-                        for (int c = 0; c < 4; ++c)
+                            for (int c = 0; c < 4; ++c)
 #pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                if (32 * c + j >= valid) r[c][j] = __float_as_uint(-INFINITY);
+                                for (int j = 0; j < 32; ++j)
+                                    if (!((vmask[c] >> j) & 1u)) r[c][j] = __float_as_uint(-INFINITY);
+                        }
+                    } else {
+                        const int valid = min(max(n_ctx - t * T, 0), T);  // tokens of this tile inside the context
+                        if (valid < T) {  // tail tile (warp-uniform): mask the tokens past the context
+#pragma unroll
+                            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    if (32 * c + j >= valid) r[c][j] = __float_as_uint(-INFINITY);
+                        }
                     }
                     // row max of the raw scores (scale > 0): eight independent chains of
                     // three-operand max, then a short tree
@@ -458,7 +572,10 @@ bool encode_map(CUtensorMap *map, const void *base, int rank, const cuuint64_t *
 
 bool tc_supported(const VerifyArgs &a) {
     // the softmax takes the row max of the raw scores, which needs scale > 0
-    return a.L >= 1 && a.G >= 1 && a.G <= 128 && (128 % a.G) == 0 && !a.idx && a.scale > 0.f;
+    if (!(a.G >= 1 && a.G <= 128 && (128 % a.G) == 0 && a.scale > 0.f)) return false;
+    if (a.idx)  // gathered rows are copied 16 bytes at a time: every row start 16-byte aligned
+        return a.budget >= 1 && a.sb % 8 == 0 && a.sh % 8 == 0 && a.st % 8 == 0;
+    return a.L >= 1;
 }
 
 cudaError_t launch_cache_attn_tc(const VerifyArgs &a, const SplitPlan &p, cudaStream_t s, cudaEvent_t ev0,
@@ -471,7 +588,11 @@ cudaError_t launch_cache_attn_tc(const VerifyArgs &a, const SplitPlan &p, cudaSt
         const cuuint32_t box[3] = {64, (cuuint32_t)a.G, (cuuint32_t)(128 / a.G)};
         if (!encode_map(&mq, a.q, 3, dims, strides, box)) return cudaSuccess;
     }
-    {
+    const bool sparse = a.idx != nullptr;
+    if (sparse) {  // rows are gathered with cp.async; the K/V maps are not read
+        mk = mq;
+        mv = mq;
+    } else {
         const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)a.L, (cuuint64_t)a.Hkv, (cuuint64_t)a.B};
         const cuuint64_t strides[3] = {(cuuint64_t)a.st * 2, (cuuint64_t)a.sh * 2, (cuuint64_t)a.sb * 2};
         const cuuint32_t box[4] = {64, (cuuint32_t)T, 1, 1};
@@ -481,10 +602,11 @@ cudaError_t launch_cache_attn_tc(const VerifyArgs &a, const SplitPlan &p, cudaSt
     TcParams tp;
     tp.M = a.G * a.N;
     tp.split_tiles = tp.M <= 128 ? 1 : 0;
-    cudaError_t e = cudaFuncSetAttribute(cache_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    auto kern = sparse ? cache_attn_tc_kernel<true> : cache_attn_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (ev0) cudaEventRecord(ev0, s);
-    cache_attn_tc_kernel<<<p.ctas, THREADS, SMEM_BYTES, s>>>(a, p, tp, mq, mk, mv);
+    kern<<<p.ctas, THREADS, SMEM_BYTES, s>>>(a, p, tp, mq, mk, mv);
     e = cudaGetLastError();
     if (ev1) cudaEventRecord(ev1, s);
     count_launches(1);

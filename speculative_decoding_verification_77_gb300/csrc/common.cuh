@@ -139,6 +139,40 @@ __device__ __forceinline__ int context_len(const VerifyArgs &a, int b) {
     return n;
 }
 
+// Token behind index slot j of sequence b in sparse mode, or -1 when the slot
+// is unused: past the budget, -1 padding, outside [0, n), or not above the
+// previous slot's token. Unused entries other than -1 padding are bad input.
+__device__ __forceinline__ int sparse_token(const VerifyArgs &a, int b, int n, int j, bool report) {
+    if (j >= a.budget) return -1;
+    const int32_t *ib = a.idx + (int64_t)b * a.budget;
+    const int t = __ldg(ib + j);
+    const bool ok = t >= 0 && t < n && (j == 0 || t > __ldg(ib + j - 1));
+    if (!ok && t != -1 && report) flag_status(a.status, SPEC_ERR_BAD_INPUT);
+    return ok ? t : -1;
+}
+
+// The same rule split in two, so that the loads can be issued a tile early:
+// the raw entries of slot j and of slot j - 1 ...
+struct IdxPair {
+    int cur, prev;
+};
+__device__ __forceinline__ IdxPair sparse_raw(const VerifyArgs &a, int b, int j) {
+    IdxPair r{-1, -1};
+    if (j < a.budget) {
+        const int32_t *ib = a.idx + (int64_t)b * a.budget;
+        r.cur = __ldg(ib + j);
+        r.prev = j > 0 ? __ldg(ib + j - 1) : -1;
+    }
+    return r;
+}
+// ... then the token (or -1) once they have arrived.
+__device__ __forceinline__ int sparse_resolve(const VerifyArgs &a, IdxPair r, int j, int n, bool report) {
+    if (j >= a.budget) return -1;
+    const bool ok = r.cur >= 0 && r.cur < n && (j == 0 || r.cur > r.prev);
+    if (!ok && r.cur != -1 && report) flag_status(a.status, SPEC_ERR_BAD_INPUT);
+    return ok ? r.cur : -1;
+}
+
 // Tiling of the mma.sync cache kernel (query rows per unit, tokens per tile).
 int mma_rows_per_unit();
 int mma_tile_tokens();

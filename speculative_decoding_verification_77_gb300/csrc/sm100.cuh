@@ -232,6 +232,24 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// ---- cp.async (16-byte copies global -> shared, zero-filled when !valid) ----
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void *src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_group() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+// arrive on `bar` (counting as one of its expected arrivals) once every cp.async
+// this thread issued before has landed
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// make this thread's completed generic-proxy writes to shared memory visible to
+// the async proxy (the tensor core reads its operands through it)
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // ---- thread-block clusters and distributed shared memory ----
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;

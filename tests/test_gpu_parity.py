@@ -274,6 +274,63 @@ def test_sparse_ragged_selection(ops):
     assert_attn_close(out, lse, ro, rl)
 
 
+@pytest.mark.parametrize("case", ["g3_warp_kernel", "token_major", "padding_runs", "row_groups", "one_tile"])
+def test_sparse_paths(ops, case):
+    """Sparse verify on both cache kernels and on the index patterns each must mask."""
+    shapes = {"g3_warp_kernel": dict(B=2, N=7, Hq=12, Hkv=4, L=3000),  # G = 3: warp-level kernel
+              "token_major": dict(B=2, N=5, Hq=8, Hkv=4, L=2500),
+              "padding_runs": dict(B=2, N=5, Hq=8, Hkv=2, L=2500),
+              "row_groups": dict(B=2, N=40, Hq=16, Hkv=2, L=2600),  # G*N = 320 rows: three row groups
+              "one_tile": dict(B=1, N=3, Hq=4, Hkv=1, L=90)}[case]
+    x = small(77, depth=5, **shapes)
+    B, L = shapes["B"], shapes["L"]
+    ds, ts = W.random_scores(B, L, seed=11)
+    budget = 80 if case == "one_tile" else 700
+    kw = dict(sink=4, window=32, top_m=200 if budget > 100 else 20, budget=budget)
+    ridx, _, st = oracle.select(ds, ts, **kw)
+    assert st == 0
+    if case == "padding_runs":  # unused slots inside the list: -1 runs, a repeat, an out-of-range entry
+        ridx = ridx.copy()
+        ridx[0, 100:230] = -1
+        ridx[1, 128:256] = -1
+        ridx[1, 300] = ridx[1, 299]
+        ridx[1, 400] = L + 5
+    idx = torch.from_numpy(ridx)
+    g = to_dev(x)
+    k, v = g["k_cache"], g["v_cache"]
+    if case == "token_major":
+        k = x["k_cache"].permute(0, 2, 1, 3).contiguous().to(dev()).permute(0, 2, 1, 3)
+        v = x["v_cache"].permute(0, 2, 1, 3).contiguous().to(dev()).permute(0, 2, 1, 3)
+    out, lse = ops.verify_attn_sparse(g["q"], k, v, g["k_draft"], g["v_draft"], g["parent"], idx.to(dev()),
+                                      scale=x["scale"])
+    ro, rl, st = oracle.attend(x["q"], x["k_cache"], x["v_cache"], x["k_draft"], x["v_draft"], x["parent"],
+                               scale=x["scale"], idx=idx)
+    assert st == (5 if case == "padding_runs" else 0)
+    torch.cuda.synchronize()
+    assert_attn_close(out, lse, ro, rl)
+
+
+@pytest.mark.parametrize("slot", [0, 127, 128, 255, 1999])
+def test_sparse_needle_at_index_slot(ops, slot):
+    """A key with logit ~ +30 behind index slot `slot`: o must be that key's V."""
+    x = small(300 + slot, B=1, N=2, Hq=4, Hkv=2, L=9000)
+    idx = torch.from_numpy(np.sort(np.random.default_rng(slot).choice(9000, size=2000, replace=False))
+                           .astype(np.int32))[None]
+    t = int(idx[0, slot])
+    qv = x["q"][0, 1, 3].double()
+    x["k_cache"][0, 1, t] = (qv * (30.0 / (x["scale"] * float(qv.dot(qv))))).to(torch.bfloat16)
+    g = to_dev(x)
+    out, lse = ops.verify_attn_sparse(g["q"], g["k_cache"], g["v_cache"], g["k_draft"], g["v_draft"],
+                                      g["parent"], idx.to(dev()), scale=x["scale"])
+    rows = np.array([1 * 4 + 3])
+    ro, rl, _ = oracle.attend(x["q"], x["k_cache"], x["v_cache"], x["k_draft"], x["v_draft"], x["parent"],
+                              scale=x["scale"], idx=idx, rows=rows)
+    torch.cuda.synchronize()
+    o = out.cpu().numpy().reshape(-1, 128)[rows[0]]
+    assert np.abs(o - x["v_cache"][0, 1, t].float().numpy()).max() < 2e-2
+    assert_attn_close(out, lse, ro, rl, rows)
+
+
 @pytest.mark.parametrize("case", ["ties", "special", "small_ctx", "big_top_m", "zero_top_m"])
 def test_selection_cases_bit_exact(ops, case):
     B, L = 5, 5000
