@@ -38,9 +38,13 @@ METRIC = "verify-attention µs/step and achieved HBM TB/s (% of 8 TB/s) at B=4, 
 L2_BYTES = 129 * 1000 * 1000
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM bytes per launch of the cache kernel from one ncu capture, keyed by the
-# sha256 of the kernel source it was taken on; a changed kernel reports null.
-NCU_TRAFFIC = {}
+# DRAM bytes (read + written) per launch of the cache kernel from one ncu
+# capture, keyed by the sha256 of the kernel source it was taken on and the
+# workload; a changed kernel reports null. The capture and its command are
+# summarised in profiles/cache_attn_tc_llama3-8b-layer_ncu.md.
+NCU_TRAFFIC = {
+    ("366fb684634d6190", "llama3-8b-layer-B4-L32k-N64-tree"): 541_603_840 + 8_358_656,
+}
 
 
 def kernel_source_hash() -> str:
@@ -296,7 +300,7 @@ def finish(args, ws_, rank, w, ms, ms_max, kd_ms, launches, h2d, d2h, e2e_ms, cl
     peaks, peak_src = measured_peaks()
     kv = w.kv_bytes()
     achieved_gbs = kv / (kd_ms * 1e-3) / 1e9
-    traffic = NCU_TRAFFIC.get(kernel_source_hash())
+    traffic = NCU_TRAFFIC.get((kernel_source_hash(), w.name))
     rec = {
         "metric": METRIC,
         "value": round(kv * ws_ / (ms_max * 1e-3) / 1e12, 4),
@@ -345,7 +349,7 @@ def config_of(w, ws_, kv, flush):
 
 def kernel_name(w):
     if w.sparse:
-        return "cache_attn_mma<sparse> (mma.sync index gather)"
+        return "cache_attn_tc<sparse> (tcgen05, cp.async row gather)"
     return "cache_attn_tc (tcgen05 split-KV)"
 
 

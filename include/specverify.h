@@ -201,6 +201,10 @@ spec_status_t spec_verify_attn_noalloc(const uint16_t *q, const uint16_t *k_cach
  * SPEC_ERR_TIMEOUT from a bounded wait that gave up). */
 spec_status_t spec_read_device_status(const void *workspace, void *stream);
 
+/* Text of the CUDA error behind the last SPEC_ERR_CUDA this host thread got
+ * from the library ("no error" if none). The string is static; do not free. */
+const char *spec_last_cuda_error(void);
+
 /* ------------------------------------------------------------------------ */
 /* Measurement aids (per calling thread; not needed for normal use).
  *

@@ -11,6 +11,7 @@ namespace {
 thread_local uint64_t g_launches = 0;
 thread_local cudaEvent_t g_prof_start = nullptr;
 thread_local cudaEvent_t g_prof_stop = nullptr;
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
 
 constexpr int kMaxDevices = 64;
 struct DeviceInfo {
@@ -115,7 +116,7 @@ spec_status_t verify_common(const uint16_t *q, const uint16_t *k_cache, const ui
     a.status = reinterpret_cast<uint32_t *>(ws);
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (const cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s); e != cudaSuccess) return (spec_status_t)cuda_failure(e);
     cudaEvent_t ev0 = g_prof_start && g_prof_stop ? g_prof_start : nullptr;
     cudaEvent_t ev1 = ev0 ? g_prof_stop : nullptr;
     // the tcgen05 kernel when the shape allows it (its TMA maps, its 16-byte row gathers);
@@ -126,21 +127,26 @@ spec_status_t verify_common(const uint16_t *q, const uint16_t *k_cache, const ui
         plan = make_plan_tc(B, N, Hq, Hkv, L_eff, dev.sms);
         a.o_part = reinterpret_cast<float *>(ws + kHeaderBytes);
         a.lse_part = reinterpret_cast<float *>(ws + kHeaderBytes + plan_o_bytes(plan, d));
-        if (launch_cache_attn_tc(a, plan, s, ev0, ev1, &launched) != cudaSuccess) return SPEC_ERR_CUDA;
+        if (const cudaError_t e = launch_cache_attn_tc(a, plan, s, ev0, ev1, &launched); e != cudaSuccess) return (spec_status_t)cuda_failure(e);
     }
     if (!launched) {
         plan = verify_plan(B, N, Hq, Hkv, L_eff, dev.sms);
         a.o_part = reinterpret_cast<float *>(ws + kHeaderBytes);
         a.lse_part = reinterpret_cast<float *>(ws + kHeaderBytes + plan_o_bytes(plan, d));
-        if (launch_cache_attn_mma(a, plan, sparse, s, ev0, ev1) != cudaSuccess) return SPEC_ERR_CUDA;
+        if (const cudaError_t e = launch_cache_attn_mma(a, plan, sparse, s, ev0, ev1); e != cudaSuccess) return (spec_status_t)cuda_failure(e);
     }
-    if (launch_merge_tree(a, plan, s) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (const cudaError_t e = launch_merge_tree(a, plan, s); e != cudaSuccess) return (spec_status_t)cuda_failure(e);
     return SPEC_OK;
 }
 
 }  // namespace
 
 void count_launches(int n) { g_launches += (uint64_t)n; }
+
+int cuda_failure(cudaError_t e) {
+    g_last_cuda_error = e;
+    return SPEC_ERR_CUDA;
+}
 
 }  // namespace specverify
 
@@ -182,10 +188,11 @@ spec_status_t spec_select_topk(const float *draft_score, const float *target_sco
     if (spec_status_t s = current_device(&dev)) return s;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint32_t *status = static_cast<uint32_t *>(workspace);
-    if (cudaMemsetAsync(status, 0, sizeof(uint32_t), s) != cudaSuccess) return SPEC_ERR_CUDA;
-    if (launch_select_topk(draft_score, target_score, ld, B, L, ctx_lens, sink, window, top_m, budget,
-                           idx, count, status, s) != cudaSuccess)
-        return SPEC_ERR_CUDA;
+    if (const cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s); e != cudaSuccess) return (spec_status_t)cuda_failure(e);
+    if (const cudaError_t e = launch_select_topk(draft_score, target_score, ld, B, L, ctx_lens, sink, window,
+                                                 top_m, budget, idx, count, status, s);
+        e != cudaSuccess)
+        return (spec_status_t)cuda_failure(e);
     return SPEC_OK;
 }
 
@@ -229,9 +236,10 @@ spec_status_t spec_lse_merge(const float *o_a, const float *lse_a, const float *
     if (rows > ((int64_t)1 << 36)) return SPEC_ERR_INVALID_ARG;
     DeviceInfo dev;
     if (spec_status_t s = current_device(&dev)) return s;
-    if (launch_lse_merge2(o_a, lse_a, o_b, lse_b, out, lse_out, rows, d,
-                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return SPEC_ERR_CUDA;
+    if (const cudaError_t e = launch_lse_merge2(o_a, lse_a, o_b, lse_b, out, lse_out, rows, d,
+                                               static_cast<cudaStream_t>(stream));
+        e != cudaSuccess)
+        return (spec_status_t)cuda_failure(e);
     return SPEC_OK;
 }
 
@@ -239,10 +247,14 @@ spec_status_t spec_read_device_status(const void *workspace, void *stream) {
     if (!workspace) return SPEC_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint32_t v = 0;
-    if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return SPEC_ERR_CUDA;
-    if (cudaStreamSynchronize(s) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (const cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, s); e != cudaSuccess)
+        return (spec_status_t)cuda_failure(e);
+    if (const cudaError_t e = cudaStreamSynchronize(s); e != cudaSuccess) return (spec_status_t)cuda_failure(e);
     return static_cast<spec_status_t>(v);
+}
+
+const char *spec_last_cuda_error(void) {
+    return g_last_cuda_error == cudaSuccess ? "no error" : cudaGetErrorString(g_last_cuda_error);
 }
 
 void spec_profile_events(void *start_event, void *stop_event) {

@@ -76,6 +76,8 @@ struct Bars {
     uint32_t tmem_base;
     uint32_t abort;
 };
+static_assert(sizeof(Bars) <= 256, "barrier block fits its reservation");
+static_assert(SMEM_BYTES <= 232448, "dynamic shared memory fits one CTA per SM");
 
 struct TcParams {
     int split_tiles;  // 1: pipes take alternate tiles of the same <=128 rows
@@ -137,6 +139,7 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
                      const __grid_constant__ CUtensorMap tm_v) {
     extern __shared__ uint8_t smem_raw[];
     griddep_launch_dependents();  // the merge may be scheduled as this grid's CTAs drain
+    // the 128-byte swizzle needs 1024-byte aligned tiles; SMEM_BYTES has 1 KiB of slack for it
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint8_t *sQ = smem;
     uint8_t *sRing = smem + SMEM_RING;

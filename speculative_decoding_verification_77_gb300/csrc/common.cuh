@@ -177,6 +177,10 @@ __device__ __forceinline__ int sparse_resolve(const VerifyArgs &a, IdxPair r, in
 int mma_rows_per_unit();
 int mma_tile_tokens();
 
+// Records a failed CUDA call for spec_last_cuda_error() (this host thread) and
+// returns SPEC_ERR_CUDA.
+int cuda_failure(cudaError_t e);
+
 // Host-side launchers (one per translation unit).
 cudaError_t launch_cache_attn_mma(const VerifyArgs &a, const SplitPlan &p, bool sparse,
                                   cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1);

@@ -87,7 +87,8 @@ extern "C" spec_status_t spec_verify_attn_noalloc(
     if (plan_workspace_bytes(plan, d) > kNoAllocScratchBytes) return SPEC_ERR_WORKSPACE;
 
     void *base = nullptr;
-    if (scratch_address(dev, &base) != cudaSuccess || base == nullptr) return SPEC_ERR_CUDA;
+    if (const cudaError_t e = scratch_address(dev, &base); e != cudaSuccess) return (spec_status_t)cuda_failure(e);
+    if (base == nullptr) return SPEC_ERR_CUDA;
     uint8_t *ws = static_cast<uint8_t *>(base);
 
     VerifyArgs a;
@@ -113,11 +114,13 @@ extern "C" spec_status_t spec_verify_attn_noalloc(
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // the scratch keeps the previous call's contents: the status word must start at zero;
     // every partial slot the merge reads is written by this call's cache kernel first
-    if (cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s) != cudaSuccess) return SPEC_ERR_CUDA;
-    if (launch_cache_attn_mma(a, plan, false, s, nullptr, nullptr) != cudaSuccess) return SPEC_ERR_CUDA;
-    if (launch_merge_tree(a, plan, s) != cudaSuccess) return SPEC_ERR_CUDA;
-    if (status_out &&
-        cudaMemcpyAsync(status_out, a.status, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
-        return SPEC_ERR_CUDA;
+    if (const cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s); e != cudaSuccess) return (spec_status_t)cuda_failure(e);
+    if (const cudaError_t e = launch_cache_attn_mma(a, plan, false, s, nullptr, nullptr); e != cudaSuccess) return (spec_status_t)cuda_failure(e);
+    if (const cudaError_t e = launch_merge_tree(a, plan, s); e != cudaSuccess) return (spec_status_t)cuda_failure(e);
+    if (status_out) {
+        if (const cudaError_t e = cudaMemcpyAsync(status_out, a.status, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s);
+            e != cudaSuccess)
+            return (spec_status_t)cuda_failure(e);
+    }
     return SPEC_OK;
 }

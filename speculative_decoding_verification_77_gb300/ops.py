@@ -25,6 +25,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libspecverify.so")
 
 SPEC_OK = 0
+SPEC_ERR_CUDA = 3
 SPEC_ERR_BAD_INPUT = 5
 STATUS_NAMES = {0: "SPEC_OK", 1: "SPEC_ERR_INVALID_ARG", 2: "SPEC_ERR_UNSUPPORTED", 3: "SPEC_ERR_CUDA",
                 4: "SPEC_ERR_WORKSPACE", 5: "SPEC_ERR_BAD_INPUT", 6: "SPEC_ERR_TIMEOUT"}
@@ -44,14 +45,15 @@ SIGNATURES = {
     "spec_read_device_status": (I, [P, P]),
     "spec_profile_events": (None, [P, P]),
     "spec_kernel_launches": (ctypes.c_uint64, []),
+    "spec_last_cuda_error": (ctypes.c_char_p, []),
 }
 
 _lib = None
 
 
 class SpecError(RuntimeError):
-    def __init__(self, fn: str, code: int):
-        super().__init__(f"{fn} failed: {STATUS_NAMES.get(code, code)}")
+    def __init__(self, fn: str, code: int, detail: str = ""):
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(code, code)}" + (f" ({detail})" if detail else ""))
         self.code = code
 
 
@@ -72,7 +74,8 @@ def load_library(path: str = LIB_PATH):
 
 def _check(fn: str, code: int):
     if code != SPEC_OK:
-        raise SpecError(fn, code)
+        detail = _lib.spec_last_cuda_error().decode() if code == SPEC_ERR_CUDA and _lib is not None else ""
+        raise SpecError(fn, code, detail)
 
 
 def _ptr(t: torch.Tensor | None):

@@ -47,6 +47,7 @@ def test_status_strings(lib):
     assert lib.spec_status_string(0) == b"SPEC_OK"
     assert lib.spec_status_string(5) == b"SPEC_ERR_BAD_INPUT"
     assert lib.spec_status_string(99) == b"SPEC_ERR_UNKNOWN"
+    assert lib.spec_last_cuda_error() == b"no error"  # nothing has failed in this thread
 
 
 def test_workspace_sizes(lib):
