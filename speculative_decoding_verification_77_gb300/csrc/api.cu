@@ -9,6 +9,7 @@ namespace specverify {
 namespace {
 
 thread_local uint64_t g_launches = 0;
+
 thread_local cudaEvent_t g_prof_start = nullptr;
 thread_local cudaEvent_t g_prof_stop = nullptr;
 thread_local cudaError_t g_last_cuda_error = cudaSuccess;
@@ -62,7 +63,8 @@ SplitPlan verify_plan(int B, int N, int Hq, int Hkv, int L_eff, int sms) {
 // Workspace that covers either cache kernel's plan.
 size_t verify_bytes_any(int B, int N, int Hq, int Hkv, int d, int L_eff, int sms) {
     const size_t a = plan_workspace_bytes(verify_plan(B, N, Hq, Hkv, L_eff, sms), d);
-    const size_t b = plan_workspace_bytes(make_plan_tc(B, N, Hq, Hkv, L_eff, sms), d);
+    // the slot count does not depend on balancing, so the dense plan sizes both kinds
+    const size_t b = plan_workspace_bytes(make_plan_tc(B, N, Hq, Hkv, L_eff, sms, false), d);
     return a > b ? a : b;
 }
 
@@ -124,7 +126,7 @@ spec_status_t verify_common(const uint16_t *q, const uint16_t *k_cache, const ui
     SplitPlan plan;
     bool launched = false;
     if (tc_supported(a)) {
-        plan = make_plan_tc(B, N, Hq, Hkv, L_eff, dev.sms);
+        plan = make_plan_tc(B, N, Hq, Hkv, L_eff, dev.sms, sparse);
         a.o_part = reinterpret_cast<float *>(ws + kHeaderBytes);
         a.lse_part = reinterpret_cast<float *>(ws + kHeaderBytes + plan_o_bytes(plan, d));
         if (const cudaError_t e = launch_cache_attn_tc(a, plan, s, ev0, ev1, &launched); e != cudaSuccess) return (spec_status_t)cuda_failure(e);

@@ -69,7 +69,7 @@ constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 128, true);
 constexpr long long WAIT_LIMIT_CYCLES = 4000000000LL;  // ~2 s
 
 struct Bars {
-    uint64_t q_full, q_empty;
+    uint64_t q_full[2], q_empty[2];  // Q buffers (two only when the pipes share <= 128 rows)
     uint64_t kv_full[RING], kv_empty[RING];
     uint64_t s_full[2], p_full[2], o_done[2], o_empty[2];
     uint64_t mma_done;
@@ -132,6 +132,41 @@ __device__ __forceinline__ int seg_tile(const Seg &s, int split_tiles, int h, in
     return split_tiles ? s.tb + 2 * i + h : s.tb + i;
 }
 
+// Q buffers: with more than 128 rows per unit the pipes read rows 0-127 and
+// 128-255 of one 64 KiB buffer; with at most 128 they share rows 0-127, and the
+// two 32 KiB halves serve alternate units, so that the next unit's Q loads while
+// the current one is still in use. Segment seg_i uses buffer seg_i % nqb for the
+// (seg_i / nqb)-th time.
+__device__ __forceinline__ void q_buffer(int split_tiles, int seg_i, int &qb, uint32_t &use) {
+    const int nqb = split_tiles ? 2 : 1;
+    qb = seg_i % nqb;
+    use = (uint32_t)(seg_i / nqb);
+}
+
+// TMA of the unit's Q rows into buffer qb (one thread).
+__device__ __forceinline__ void load_q(const CUtensorMap *tm_q, uint8_t *sQ, uint64_t *bar, int split_tiles, int qb,
+                                       const Seg &s, int BM, int G, int N) {
+    const int npipe_q = split_tiles ? 1 : 2;
+    mbar_arrive_expect_tx(bar, npipe_q * 2 * 16384);
+    for (int h = 0; h < npipe_q; ++h) {
+        const int n0 = (s.rg * BM + 128 * h) / G;
+        const int half = split_tiles ? qb : h;  // 16 KiB row block inside each 32 KiB column half
+        for (int kh = 0; kh < 2; ++kh)
+            tma_load_3d(sQ + kh * 32768 + half * 16384, tm_q, bar, kh * 64, s.hk * G, s.b * N + n0);
+    }
+}
+
+// Drain (one thread): the Q loads still in flight, the last of each buffer.
+__device__ __forceinline__ void drain_q(Bars &bs, int split_tiles, int q_loads) {
+    const int nqb = split_tiles ? 2 : 1;
+    for (int i = q_loads > nqb ? q_loads - nqb : 0; i < q_loads; ++i) {
+        int qb;
+        uint32_t quse;
+        q_buffer(split_tiles, i, qb, quse);
+        drain_wait(&bs.q_full[qb], quse & 1);
+    }
+}
+
 template <bool SPARSE>
 __global__ void __launch_bounds__(THREADS, 1)
 cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
@@ -150,8 +185,10 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
     const int BM = p.BM;
 
     if (threadIdx.x == 0) {
-        mbar_init(&bs.q_full, 1);
-        mbar_init(&bs.q_empty, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bs.q_full[i], 1);
+            mbar_init(&bs.q_empty[i], 1);
+        }
         for (int i = 0; i < RING; ++i) {
             mbar_init(&bs.kv_full[i], SPARSE ? 32 : 1);  // sparse: one arrival per gathering lane
             mbar_init(&bs.kv_empty[i], 1);
@@ -182,7 +219,7 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
         // ------------------------------------------------------------ gather producer
         if (lane == 0) tma_prefetch_desc(&tm_q);
         int64_t item = 0;  // K/V tiles issued (same in all lanes)
-        int seg_i = 0, q_loads = 0;
+        int seg_i = 0;
         bool ok = true;
         // Copy pattern: in step v (0..31), lane l copies 16-byte chunk c = l & 7 of both
         // 128-byte halves of tile row r = 4v + (l >> 3): every instruction moves four whole
@@ -194,19 +231,15 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
         for (int64_t u = u_first; ok && u * p.tiles_per_unit < g1; ++u, ++seg_i) {
             Seg s;
             seg_decode(a, p, split_tiles, u, g0, g1, s);
-            if (seg_i > 0 && !(ok = __all_sync(0xffffffffu, wait_bar(bs, &bs.q_empty, (seg_i - 1) & 1, a.status))))
-                break;
-            if (lane == 0) {
-                const int npipe_q = split_tiles ? 1 : 2;
-                mbar_arrive_expect_tx(&bs.q_full, npipe_q * 2 * 16384);
-                for (int h = 0; h < npipe_q; ++h) {
-                    const int n0 = (s.rg * BM + 128 * h) / a.G;
-                    for (int kh = 0; kh < 2; ++kh)
-                        tma_load_3d(sQ + kh * 32768 + h * 16384, &tm_q, &bs.q_full, kh * 64, s.hk * a.G,
-                                    s.b * a.N + n0);
-                }
+            {  // the unit's Q rows, as in the dense producer
+                int qb;
+                uint32_t quse;
+                q_buffer(split_tiles, seg_i, qb, quse);
+                if (quse > 0 &&
+                    !(ok = __all_sync(0xffffffffu, wait_bar(bs, &bs.q_empty[qb], (quse - 1) & 1, a.status))))
+                    break;
+                if (lane == 0) load_q(&tm_q, sQ, &bs.q_full[qb], split_tiles, qb, s, BM, a.G, a.N);
             }
-            ++q_loads;
             const int n_ctx = context_len(a, s.b);
             const char *kbase = reinterpret_cast<const char *>(a.k_cache + s.b * a.sb + s.hk * a.sh);
             const char *vbase = reinterpret_cast<const char *>(a.v_cache + s.b * a.sb + s.hk * a.sh);
@@ -246,7 +279,7 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
             }
         }
         cp_async_wait_all();  // the drain: no copy is left in flight
-        if (lane == 0 && q_loads > 0) drain_wait(&bs.q_full, (q_loads - 1) & 1);
+        if (lane == 0) drain_q(bs, split_tiles, seg_i);
         __syncwarp();
     } else if (warp == WARP_PRODUCER) {
         // ------------------------------------------------------------ TMA producer
@@ -255,22 +288,18 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
             int64_t item = 0;  // K/V tiles loaded so far (K and V count separately)
-            int seg_i = 0, q_loads = 0;
+            int q_loads = 0;
             bool ok = true;
-            for (int64_t u = u_first; ok && u * p.tiles_per_unit < g1; ++u, ++seg_i) {
+            for (int64_t u = u_first; ok && u * p.tiles_per_unit < g1; ++u, ++q_loads) {
                 Seg s;
                 seg_decode(a, p, split_tiles, u, g0, g1, s);
-                // Q rows of this unit, once the previous unit's QK MMAs are done with them
-                if (seg_i > 0 && !(ok = wait_bar(bs, &bs.q_empty, (seg_i - 1) & 1, a.status))) break;
-                const int npipe_q = split_tiles ? 1 : 2;
-                mbar_arrive_expect_tx(&bs.q_full, npipe_q * 2 * 16384);
-                ++q_loads;
-                for (int h = 0; h < npipe_q; ++h) {
-                    const int n0 = (s.rg * BM + 128 * h) / a.G;
-                    for (int kh = 0; kh < 2; ++kh)
-                        tma_load_3d(sQ + kh * 32768 + h * 16384, &tm_q, &bs.q_full, kh * 64, s.hk * a.G,
-                                    s.b * a.N + n0);
-                }
+                // the unit's Q rows, once the QK MMAs of the unit that last used the buffer are
+                // done with it (the previous unit, or with two buffers the one before)
+                int qb;
+                uint32_t quse;
+                q_buffer(split_tiles, q_loads, qb, quse);
+                if (quse > 0 && !(ok = wait_bar(bs, &bs.q_empty[qb], (quse - 1) & 1, a.status))) break;
+                load_q(&tm_q, sQ, &bs.q_full[qb], split_tiles, qb, s, BM, a.G, a.N);
                 // K and V tiles in order: tile tb: K, V; tile tb+1: K, V; ...
                 for (int t = s.tb; t < s.te; ++t) {
                     for (int kv = 0; kv < 2; ++kv, ++item) {
@@ -290,7 +319,7 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
             // drain: wait for the last copies still in flight (consumed ones return at once)
             const int64_t first = item > RING ? item - RING : 0;
             for (int64_t n = first; n < item; ++n) drain_wait(&bs.kv_full[n % RING], (uint32_t)((n / RING) & 1));
-            if (q_loads > 0) drain_wait(&bs.q_full, (q_loads - 1) & 1);
+            drain_q(bs, split_tiles, q_loads);
         }
         __syncwarp();
     } else if (warp == WARP_MMA) {
@@ -305,14 +334,19 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
             bool ok = true;
             // Descriptors are built once; every MMA only adds compile-time offsets (16-byte
             // units), which keeps the single issuing thread's instruction stream short.
-            const uint64_t dq0 = desc_sw128(smem_u32(sQ), 16, 1024);
-            const uint64_t dq1 = split_tiles ? dq0 : dq0 + (16384u >> 4);
+            const uint64_t dq_base = desc_sw128(smem_u32(sQ), 16, 1024);
             const uint64_t dk0 = desc_sw128(smem_u32(sRing), 16, 1024);
             const uint64_t dv0 = desc_sw128(smem_u32(sRing), 16384, 1024);
             for (int64_t u = u_first; ok && u * p.tiles_per_unit < g1; ++u, ++seg_i) {
                 Seg s;
                 seg_decode(a, p, split_tiles, u, g0, g1, s);
-                if (!(ok = __all_sync(0xffffffffu, wait_bar(bs, &bs.q_full, seg_i & 1, a.status)))) break;
+                int qb;
+                uint32_t quse;
+                q_buffer(split_tiles, seg_i, qb, quse);
+                if (!(ok = __all_sync(0xffffffffu, wait_bar(bs, &bs.q_full[qb], quse & 1, a.status)))) break;
+                // Q of pipe h: its own 128-row block (more than 128 rows) or this unit's buffer
+                const uint64_t dq0 = dq_base + (split_tiles ? (uint64_t)qb * (16384u >> 4) : 0u);
+                const uint64_t dq1 = split_tiles ? dq0 : dq_base + (16384u >> 4);
                 tc_fence_after();
                 const int qk_total = s.cnt[0] + s.cnt[1];
                 int qk_done = 0;
@@ -332,7 +366,7 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
                                dk + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2), IDESC_QK, ks > 0 ? 1u : 0u);
                     mma_commit_elect(&bs.s_full[h]);
                     if (split_tiles || h == 1) mma_commit_elect(&bs.kv_empty[slot]);
-                    if (++qk_done == qk_total) mma_commit_elect(&bs.q_empty);
+                    if (++qk_done == qk_total) mma_commit_elect(&bs.q_empty[qb]);
                     return true;
                 };
                 auto issue_pv = [&](int h, int i) -> bool {
@@ -606,7 +640,9 @@ cudaError_t launch_cache_attn_tc(const VerifyArgs &a, const SplitPlan &p, cudaSt
     tp.M = a.G * a.N;
     tp.split_tiles = tp.M <= 128 ? 1 : 0;
     auto kern = sparse ? cache_attn_tc_kernel<true> : cache_attn_tc_kernel<false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    static const cudaError_t attr_dense = kernel_attributes(cache_attn_tc_kernel<false>, SMEM_BYTES);
+    static const cudaError_t attr_sparse = kernel_attributes(cache_attn_tc_kernel<true>, SMEM_BYTES);
+    cudaError_t e = sparse ? attr_sparse : attr_dense;
     if (e != cudaSuccess) return e;
     if (ev0) cudaEventRecord(ev0, s);
     kern<<<p.ctas, THREADS, SMEM_BYTES, s>>>(a, p, tp, mq, mk, mv);

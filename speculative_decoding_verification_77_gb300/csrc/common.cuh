@@ -3,6 +3,8 @@
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <algorithm>
 #include <stdint.h>
 
 #include "../../include/specverify.h"
@@ -32,12 +34,21 @@ __device__ __forceinline__ void flag_status(uint32_t *status, uint32_t code) {
 //
 // The cache part is cut into "units" (b, h_kv, row group) of up to BM query
 // rows each, every unit into tiles of `tile` KV positions. The units' tiles
-// are laid end to end (unit-major) and cut into `ctas` contiguous, balanced
-// ranges, one per CTA, so every SM gets the same number of tiles whatever B,
-// Hkv and L are. CTA c covers global tiles [start(c), start(c+1)); for each
-// unit u its range touches, it writes one normalised partial (o, lse) into
-// slot c + u. Along the range both c and u only grow, so c + u is unique per
-// (c, u) pair and the slots number ctas + units - 1.
+// are laid end to end (unit-major) and cut into `ctas` contiguous ranges, one
+// per CTA, so every SM gets about the same work whatever B, Hkv and L are.
+// CTA c covers global tiles [start(c), start(c+1)); for each unit u its range
+// touches, it writes one normalised partial (o, lse) into slot c + u. Along
+// the range both c and u only grow, so c + u is unique per (c, u) pair and the
+// slots number ctas + units - 1.
+//
+// Uniform plans give every CTA q or q + 1 tiles. Balanced plans (the tcgen05
+// kernel) charge a CTA for each extra unit its range enters, since starting a
+// unit costs about kUnitSwitchTiles tiles of time (Q reload, pipeline refill,
+// a partial written out), and cut the ranges so that tiles plus those charges
+// are even; their starts are kept in the plan.
+constexpr int kPlanMaxCtas = 512;
+constexpr int kUnitSwitchTiles = 4;
+
 struct SplitPlan {
     int BM;             // query rows per unit (rows of one CTA's tile)
     int tile;           // KV positions per tile
@@ -51,19 +62,74 @@ struct SplitPlan {
     int slot_rows;      // rows per slot
     int split_tiles;    // 1: the pipes cover alternate tiles of the same rows (both slots per row);
                         // 0: pipe h covers rows [h*slot_rows, (h+1)*slot_rows) of the unit
-    int q, rem;         // total = q * ctas + rem
+    int q, rem;         // uniform plans: total = q * ctas + rem
+    int uniform;        // 1: q / rem arithmetic; 0: the starts below
+    int32_t starts[kPlanMaxCtas + 1];  // balanced plans: start(c), start(ctas) = total
 };
 
-// CTA c covers q or q+1 tiles: the first `rem` CTAs take q+1 (q = total / ctas,
-// rem = total % ctas). All in 32-bit arithmetic (total < 2^31 is checked on the host).
+// Uniform: CTA c covers q or q+1 tiles, the first `rem` CTAs taking q+1 (q = total
+// / ctas, rem = total % ctas). All in 32-bit arithmetic (total < 2^31 is checked on
+// the host).
 __host__ __device__ __forceinline__ int64_t plan_start(const SplitPlan &p, int64_t c) {
     const int ci = (int)c;
+    if (!p.uniform) return p.starts[ci];
     return (int64_t)ci * p.q + (ci < p.rem ? ci : p.rem);
 }
+// The CTA whose range holds global tile g (0 <= g < total).
 __host__ __device__ __forceinline__ int64_t plan_cta_of(const SplitPlan &p, int64_t g) {
     const int gi = (int)g;
+    if (!p.uniform) {  // the last c with starts[c] <= g; empty ranges only follow the last tile
+        int lo = 0, hi = p.ctas - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.starts[mid] <= gi) lo = mid;
+            else hi = mid - 1;
+        }
+        return lo;
+    }
     const int big = p.rem * (p.q + 1);
     return gi < big ? gi / (p.q + 1) : p.rem + (gi - big) / p.q;
+}
+
+// Greedy cut of the tiles into contiguous ranges whose cost (tiles plus
+// kUnitSwitchTiles for every unit a range enters after its first) stays within
+// `budget`; returns the number of ranges used and fills starts[0..used).
+inline int plan_cut(int64_t total, int tiles_per_unit, int64_t budget, int max_ranges, int32_t *starts) {
+    int64_t g = 0;
+    int used = 0;
+    while (g < total) {
+        if (used == max_ranges) return max_ranges + 1;  // does not fit
+        starts[used++] = (int32_t)g;
+        int64_t cost = 0, pos = g;
+        while (pos < total) {
+            const int64_t avail = tiles_per_unit - pos % tiles_per_unit;
+            const int64_t extra = pos == g ? 0 : kUnitSwitchTiles;
+            const int64_t take = std::min<int64_t>(avail, budget - cost - extra);
+            if (take <= 0) break;
+            cost += extra + take;
+            pos += take;
+            if (take < avail) break;
+        }
+        if (pos == g) return max_ranges + 1;  // budget below one tile
+        g = pos;
+    }
+    return used;
+}
+
+// Turns a uniform plan into a balanced one: the smallest budget whose greedy cut
+// fits the plan's CTAs (trailing CTAs get empty ranges at the end).
+inline void plan_balance(SplitPlan &p) {
+    if (p.ctas > kPlanMaxCtas || p.total < 2 * (int64_t)p.ctas) return;  // too few tiles to matter
+    int64_t lo = (p.total + p.ctas - 1) / p.ctas, hi = lo + 2 * kUnitSwitchTiles + 2;
+    while (lo < hi) {
+        const int64_t mid = (lo + hi) / 2;
+        if (plan_cut(p.total, p.tiles_per_unit, mid, p.ctas, p.starts) <= p.ctas) hi = mid;
+        else lo = mid + 1;
+    }
+    const int used = plan_cut(p.total, p.tiles_per_unit, lo, p.ctas, p.starts);
+    if (used > p.ctas) return;  // keep the uniform plan
+    for (int c = used; c <= p.ctas; ++c) p.starts[c] = (int32_t)p.total;
+    p.uniform = 0;
 }
 
 inline SplitPlan make_plan(int B, int N, int Hq, int Hkv, int L_eff, int BM, int tile, int max_ctas) {
@@ -76,7 +142,9 @@ inline SplitPlan make_plan(int B, int N, int Hq, int Hkv, int L_eff, int BM, int
     p.tiles_per_unit = L_eff > 0 ? (L_eff + tile - 1) / tile : 1;
     p.total = (int64_t)p.units * p.tiles_per_unit;
     p.ctas = (int)(p.total < max_ctas ? p.total : max_ctas);
+    if (p.ctas > kPlanMaxCtas) p.ctas = kPlanMaxCtas;
     if (p.ctas < 1) p.ctas = 1;
+    p.uniform = 1;
     p.q = (int)(p.total / p.ctas);
     p.rem = (int)(p.total % p.ctas);
     p.pipes = 1;
@@ -88,13 +156,17 @@ inline SplitPlan make_plan(int B, int N, int Hq, int Hkv, int L_eff, int BM, int
 
 // Plan of the tensor-core cache kernel: units of 256 query rows (128 when G*N <= 128),
 // 128-token tiles, one CTA per SM, two pipes of 128 rows each writing their own slots.
-inline SplitPlan make_plan_tc(int B, int N, int Hq, int Hkv, int L_eff, int sms) {
+// Dense plans are balanced against the cost of entering a unit; sparse ones (gathered
+// tiles, where a unit switch costs less than the SMs a balanced cut leaves idle) stay
+// uniform.
+inline SplitPlan make_plan_tc(int B, int N, int Hq, int Hkv, int L_eff, int sms, bool sparse) {
     const int M = (Hq / Hkv) * N;
     SplitPlan p = make_plan(B, N, Hq, Hkv, L_eff, M > 128 ? 256 : 128, 128, sms);
     p.pipes = 2;
     p.slot_rows = 128;
     p.split_tiles = M <= 128 ? 1 : 0;
     p.slots = ((int64_t)p.ctas + p.units - 1) * 2;
+    if (!sparse) plan_balance(p);
     return p;
 }
 
@@ -176,6 +248,15 @@ __device__ __forceinline__ int sparse_resolve(const VerifyArgs &a, IdxPair r, in
 // Tiling of the mma.sync cache kernel (query rows per unit, tokens per tile).
 int mma_rows_per_unit();
 int mma_tile_tokens();
+
+// Kernel attributes, set once per process (the launchers keep the result in a
+// function-local static): the dynamic shared memory a kernel may use beyond the
+// 48 KiB default.
+template <class Kernel>
+cudaError_t kernel_attributes(Kernel kern, int dyn_smem) {
+    if (dyn_smem <= 48 * 1024) return cudaSuccess;
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem);
+}
 
 // Records a failed CUDA call for spec_last_cuda_error() (this host thread) and
 // returns SPEC_ERR_CUDA.

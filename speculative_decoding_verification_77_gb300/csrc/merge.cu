@@ -249,6 +249,21 @@ __global__ void __launch_bounds__(256) lse_merge2_kernel(const float *o_a, const
 
 }  // namespace
 
+// Attributes of the merge kernels, set once: shared memory for the largest N (8 warps x
+// 4096 parents) and the common carve-out.
+cudaError_t merge_attributes() {
+    constexpr int kMaxMergeSmem = 8 * 4096 * (int)sizeof(int32_t);
+    static const cudaError_t e = [] {
+        cudaError_t r = kernel_attributes(merge_tree_kernel<8>, kMaxMergeSmem);
+        if (r == cudaSuccess) r = kernel_attributes(merge_tree_kernel<4>, kMaxMergeSmem);
+        if (r == cudaSuccess) r = kernel_attributes(merge_tree_kernel<2>, kMaxMergeSmem);
+        if (r == cudaSuccess) r = kernel_attributes(merge_tree_kernel<1>, kMaxMergeSmem);
+        if (r == cudaSuccess) r = kernel_attributes(lse_merge2_kernel, 0);
+        return r;
+    }();
+    return e;
+}
+
 cudaError_t launch_merge_tree(const VerifyArgs &a, const SplitPlan &p, cudaStream_t s) {
     // heads per warp: the largest of 8, 4, 2, 1 that divides G
     const int gb = a.G % 8 == 0 ? 8 : a.G % 4 == 0 ? 4 : a.G % 2 == 0 ? 2 : 1;
@@ -265,15 +280,8 @@ cudaError_t launch_merge_tree(const VerifyArgs &a, const SplitPlan &p, cudaStrea
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaSuccess;
-    if (cfg.dynamicSmemBytes > 48 * 1024) {  // N > 1536
-        const int smem = (int)cfg.dynamicSmemBytes;
-        if (e == cudaSuccess) e = cudaFuncSetAttribute(merge_tree_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e == cudaSuccess) e = cudaFuncSetAttribute(merge_tree_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e == cudaSuccess) e = cudaFuncSetAttribute(merge_tree_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e == cudaSuccess) e = cudaFuncSetAttribute(merge_tree_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-    }
+    cudaError_t e = merge_attributes();
+    if (e != cudaSuccess) return e;
     switch (gb) {
         case 8: e = cudaLaunchKernelEx(&cfg, merge_tree_kernel<8>, a, p); break;
         case 4: e = cudaLaunchKernelEx(&cfg, merge_tree_kernel<4>, a, p); break;
@@ -288,6 +296,7 @@ cudaError_t launch_lse_merge2(const float *o_a, const float *lse_a, const float 
                               const float *lse_b, float *out, float *lse_out, int64_t rows, int d,
                               cudaStream_t s) {
     if (rows == 0) return cudaSuccess;
+    if (const cudaError_t e = merge_attributes(); e != cudaSuccess) return e;
     const int64_t blocks = (rows * 32 + 255) / 256;
     lse_merge2_kernel<<<(unsigned)blocks, 256, 0, s>>>(o_a, lse_a, o_b, lse_b, out, lse_out, rows, d);
     count_launches(1);

@@ -32,6 +32,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 2048;  // 11-bit digits
 constexpr int kSlice = kBins / kCtas;  // bins whose cluster total lives in each CTA
 constexpr int kPassesPerTier = 3;
+constexpr int kMaxL = 1572864;  // longest context the entry point accepts
 static_assert(kBins == 4 * kThreads, "four bins per thread in the digit search");
 
 // Order-preserving key: larger score -> larger key; -0 == +0; NaN -> 0, below
@@ -372,10 +373,16 @@ cudaError_t launch_select_topk(const float *ds, const float *ts, int64_t ld, int
     const bool use_staged = staged <= 200 * 1024;
     const size_t smem = use_staged ? staged : base;
     auto kern = use_staged ? select_topk_kernel<true> : select_topk_kernel<false>;
-    if (smem > 48 * 1024) {
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
+    // attributes for the largest shared memory either variant can need, set once
+    static const cudaError_t attr = [] {
+        cudaError_t e = kernel_attributes(select_topk_kernel<true>, 200 * 1024);
+        if (e == cudaSuccess) {
+            const size_t Cmax = (size_t)chunk_tokens(kMaxL);
+            e = kernel_attributes(select_topk_kernel<false>, (int)(sizeof(SelectSmem) + Cmax / 32 * sizeof(uint32_t)));
+        }
+        return e;
+    }();
+    if (attr != cudaSuccess) return attr;
     kern<<<(unsigned)B * kCtas, kThreads, smem, s>>>(ds, ts, ld, L, ctx_lens, sink, window, top_m, budget, idx,
                                                      count, status);
     count_launches(1);
