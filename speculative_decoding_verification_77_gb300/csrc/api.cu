@@ -65,7 +65,7 @@ size_t verify_bytes_any(int B, int N, int Hq, int Hkv, int d, int L_eff, int sms
     const size_t a = plan_workspace_bytes(verify_plan(B, N, Hq, Hkv, L_eff, sms), d);
     // the slot count does not depend on balancing, so the dense plan sizes both kinds
     const size_t b = plan_workspace_bytes(make_plan_tc(B, N, Hq, Hkv, L_eff, sms, false), d);
-    return a > b ? a : b;
+    return std::max(a, b);
 }
 
 spec_status_t verify_common(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,

@@ -41,22 +41,16 @@
 // Every wait on an mbarrier is bounded; a wait that gives up records
 // SPEC_ERR_TIMEOUT, the CTA drains its in-flight copies and MMAs, frees TMEM
 // and returns.
-#include <cudaTypedefs.h>
-
-#include "common.cuh"
-#include "sm100.cuh"
+#include "tc_pipe.cuh"
 
 namespace specverify {
 
 namespace {
 
 using namespace sm100;
+using namespace tcpipe;
 
 constexpr int D = kHeadDim;
-constexpr int T = 128;                // tokens per tile
-constexpr int RING = 5;               // K/V slots
-constexpr int SLOT_BYTES = T * D * 2; // 32 KiB: one K or V tile
-constexpr int HALF_BYTES = SLOT_BYTES / 2;
 constexpr int Q_BYTES = 256 * D * 2;  // 64 KiB
 constexpr int SMEM_RING = Q_BYTES;
 constexpr int SMEM_BAR = SMEM_RING + RING * SLOT_BYTES;  // 229376
@@ -66,82 +60,13 @@ constexpr int WARP_PRODUCER = 8, WARP_MMA = 9;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 128, true);
-constexpr long long WAIT_LIMIT_CYCLES = 4000000000LL;  // ~2 s
 
-struct Bars {
-    uint64_t q_full[2], q_empty[2];  // Q buffers (two only when the pipes share <= 128 rows)
-    uint64_t kv_full[RING], kv_empty[RING];
-    uint64_t s_full[2], p_full[2], o_done[2], o_empty[2];
-    uint64_t mma_done;
-    uint32_t tmem_base;
-    uint32_t abort;
-};
-static_assert(sizeof(Bars) <= 256, "barrier block fits its reservation");
 static_assert(SMEM_BYTES <= 232448, "dynamic shared memory fits one CTA per SM");
 
 struct TcParams {
     int split_tiles;  // 1: pipes take alternate tiles of the same <=128 rows
     int M;            // G * N query rows per (b, h_kv)
 };
-
-// Bounded wait: false (and the abort flag set) if the phase does not complete in time.
-__device__ __forceinline__ bool wait_bar(Bars &bs, uint64_t *bar, uint32_t parity, uint32_t *status) {
-    if (*(volatile uint32_t *)&bs.abort) return false;
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (true) {
-        if (mbar_try_wait_sleep(bar, parity, 20000)) return true;  // sleeps in hardware, no spinning
-        if (*(volatile uint32_t *)&bs.abort) return false;
-        if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
-            atomicExch(&bs.abort, 1u);
-            flag_status(status, SPEC_ERR_TIMEOUT);
-            return false;
-        }
-    }
-}
-
-// Wait used while draining after an abort: ignores the abort flag, still bounded.
-__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity) && clock64() - t0 < WAIT_LIMIT_CYCLES) {
-    }
-}
-
-// Segment of the CTA's tile range inside one unit.
-struct Seg {
-    int64_t u;
-    int tb, te;  // tiles [tb, te) of the unit
-    int b, hk, rg;
-    int cnt[2];  // tiles per pipe
-};
-
-__device__ __forceinline__ void seg_decode(const VerifyArgs &a, const SplitPlan &p, int split_tiles, int64_t u,
-                                           int64_t g0, int64_t g1, Seg &s) {
-    const int64_t ub = u * p.tiles_per_unit;
-    s.u = u;
-    s.tb = (int)((g0 > ub ? g0 : ub) - ub);
-    s.te = (int)((g1 < ub + p.tiles_per_unit ? g1 : ub + p.tiles_per_unit) - ub);
-    s.rg = (int)(u % p.row_groups);
-    s.hk = (int)((u / p.row_groups) % a.Hkv);
-    s.b = (int)(u / ((int64_t)p.row_groups * a.Hkv));
-    const int nt = s.te - s.tb;
-    s.cnt[0] = split_tiles ? (nt + 1) / 2 : nt;
-    s.cnt[1] = split_tiles ? nt / 2 : nt;
-}
-__device__ __forceinline__ int seg_tile(const Seg &s, int split_tiles, int h, int i) {
-    return split_tiles ? s.tb + 2 * i + h : s.tb + i;
-}
-
-// Q buffers: with more than 128 rows per unit the pipes read rows 0-127 and
-// 128-255 of one 64 KiB buffer; with at most 128 they share rows 0-127, and the
-// two 32 KiB halves serve alternate units, so that the next unit's Q loads while
-// the current one is still in use. Segment seg_i uses buffer seg_i % nqb for the
-// (seg_i / nqb)-th time.
-__device__ __forceinline__ void q_buffer(int split_tiles, int seg_i, int &qb, uint32_t &use) {
-    const int nqb = split_tiles ? 2 : 1;
-    qb = seg_i % nqb;
-    use = (uint32_t)(seg_i / nqb);
-}
 
 // TMA of the unit's Q rows into buffer qb (one thread).
 __device__ __forceinline__ void load_q(const CUtensorMap *tm_q, uint8_t *sQ, uint64_t *bar, int split_tiles, int qb,
@@ -153,17 +78,6 @@ __device__ __forceinline__ void load_q(const CUtensorMap *tm_q, uint8_t *sQ, uin
         const int half = split_tiles ? qb : h;  // 16 KiB row block inside each 32 KiB column half
         for (int kh = 0; kh < 2; ++kh)
             tma_load_3d(sQ + kh * 32768 + half * 16384, tm_q, bar, kh * 64, s.hk * G, s.b * N + n0);
-    }
-}
-
-// Drain (one thread): the Q loads still in flight, the last of each buffer.
-__device__ __forceinline__ void drain_q(Bars &bs, int split_tiles, int q_loads) {
-    const int nqb = split_tiles ? 2 : 1;
-    for (int i = q_loads > nqb ? q_loads - nqb : 0; i < q_loads; ++i) {
-        int qb;
-        uint32_t quse;
-        q_buffer(split_tiles, i, qb, quse);
-        drain_wait(&bs.q_full[qb], quse & 1);
     }
 }
 
@@ -215,112 +129,15 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
     const int64_t g0 = plan_start(p, blockIdx.x), g1 = plan_start(p, blockIdx.x + 1);
     const int64_t u_first = g0 / p.tiles_per_unit;
 
+    // Q of a unit into buffer qb (one thread)
+    auto qload = [&](const Seg &sg, int qb, uint64_t *bar) { load_q(&tm_q, sQ, bar, split_tiles, qb, sg, BM, a.G, a.N); };
     if (SPARSE && warp == WARP_PRODUCER) {
         // ------------------------------------------------------------ gather producer
-        if (lane == 0) tma_prefetch_desc(&tm_q);
-        int64_t item = 0;  // K/V tiles issued (same in all lanes)
-        int seg_i = 0;
-        bool ok = true;
-        // Copy pattern: in step v (0..31), lane l copies 16-byte chunk c = l & 7 of both
-        // 128-byte halves of tile row r = 4v + (l >> 3): every instruction moves four whole
-        // 128-byte lines. Row r lands at r * 128 bytes of each half, its chunks permuted by
-        // the 128-byte swizzle (c ^ (r & 7), and r & 7 = 4 (v & 1) + (l >> 3)).
-        const int rs = lane >> 3, c8 = lane & 7;
-        const uint32_t xo0 = (uint32_t)((c8 ^ rs) << 4), xo1 = (uint32_t)((c8 ^ (4 + rs)) << 4);
-        const int64_t row_bytes = a.st * 2;
-        for (int64_t u = u_first; ok && u * p.tiles_per_unit < g1; ++u, ++seg_i) {
-            Seg s;
-            seg_decode(a, p, split_tiles, u, g0, g1, s);
-            {  // the unit's Q rows, as in the dense producer
-                int qb;
-                uint32_t quse;
-                q_buffer(split_tiles, seg_i, qb, quse);
-                if (quse > 0 &&
-                    !(ok = __all_sync(0xffffffffu, wait_bar(bs, &bs.q_empty[qb], (quse - 1) & 1, a.status))))
-                    break;
-                if (lane == 0) load_q(&tm_q, sQ, &bs.q_full[qb], split_tiles, qb, s, BM, a.G, a.N);
-            }
-            const int n_ctx = context_len(a, s.b);
-            const char *kbase = reinterpret_cast<const char *>(a.k_cache + s.b * a.sb + s.hk * a.sh);
-            const char *vbase = reinterpret_cast<const char *>(a.v_cache + s.b * a.sb + s.hk * a.sh);
-            IdxPair raw[4];  // index entries of the next tile, loaded one tile ahead
-#pragma unroll
-            for (int u4 = 0; u4 < 4; ++u4) raw[u4] = sparse_raw(a, s.b, s.tb * T + 32 * u4 + lane);
-            for (int t = s.tb; ok && t < s.te; ++t) {
-                int tok[4];  // token of index slot 128 t + 32 u + lane, or -1
-#pragma unroll
-                for (int u4 = 0; u4 < 4; ++u4) tok[u4] = sparse_resolve(a, raw[u4], t * T + 32 * u4 + lane, n_ctx, true);
-                if (t + 1 < s.te) {
-#pragma unroll
-                    for (int u4 = 0; u4 < 4; ++u4) raw[u4] = sparse_raw(a, s.b, (t + 1) * T + 32 * u4 + lane);
-                }
-                int tkr[32];  // token of tile row 4v + rs, or -1
-#pragma unroll
-                for (int v = 0; v < 32; ++v) tkr[v] = __shfl_sync(0xffffffffu, tok[v >> 3], (4 * v + rs) & 31);
-                for (int kv = 0; kv < 2; ++kv) {
-                    const int slot = (int)(item % RING);
-                    const int64_t use = item / RING;
-                    if (use > 0 &&
-                        !(ok = __all_sync(0xffffffffu, wait_bar(bs, &bs.kv_empty[slot], (uint32_t)((use - 1) & 1), a.status))))
-                        break;
-                    const char *base = (kv ? vbase : kbase) + c8 * 16;
-                    const uint32_t d0 = smem_u32(sRing + slot * SLOT_BYTES) + (uint32_t)rs * 128u;
-#pragma unroll
-                    for (int v = 0; v < 32; ++v) {
-                        const bool ok_row = tkr[v] >= 0;
-                        const char *src = ok_row ? base + (int64_t)tkr[v] * row_bytes : reinterpret_cast<const char *>(a.q);
-                        const uint32_t d = d0 + (uint32_t)v * 512u + ((v & 1) ? xo1 : xo0);
-                        cp_async16_zfill(d, src, ok_row);                    // columns 0-63
-                        cp_async16_zfill(d + HALF_BYTES, src + 128, ok_row);  // columns 64-127
-                    }
-                    cp_async_mbar_arrive_noinc(&bs.kv_full[slot]);
-                    ++item;
-                }
-            }
-        }
-        cp_async_wait_all();  // the drain: no copy is left in flight
-        if (lane == 0) drain_q(bs, split_tiles, seg_i);
+        produce_sparse(bs, sRing, &tm_q, a, p, split_tiles, u_first, g0, g1, lane, qload);
         __syncwarp();
     } else if (warp == WARP_PRODUCER) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
-            int64_t item = 0;  // K/V tiles loaded so far (K and V count separately)
-            int q_loads = 0;
-            bool ok = true;
-            for (int64_t u = u_first; ok && u * p.tiles_per_unit < g1; ++u, ++q_loads) {
-                Seg s;
-                seg_decode(a, p, split_tiles, u, g0, g1, s);
-                // the unit's Q rows, once the QK MMAs of the unit that last used the buffer are
-                // done with it (the previous unit, or with two buffers the one before)
-                int qb;
-                uint32_t quse;
-                q_buffer(split_tiles, q_loads, qb, quse);
-                if (quse > 0 && !(ok = wait_bar(bs, &bs.q_empty[qb], (quse - 1) & 1, a.status))) break;
-                load_q(&tm_q, sQ, &bs.q_full[qb], split_tiles, qb, s, BM, a.G, a.N);
-                // K and V tiles in order: tile tb: K, V; tile tb+1: K, V; ...
-                for (int t = s.tb; t < s.te; ++t) {
-                    for (int kv = 0; kv < 2; ++kv, ++item) {
-                        const int slot = (int)(item % RING);
-                        const int64_t use = item / RING;
-                        if (use > 0 && !(ok = wait_bar(bs, &bs.kv_empty[slot], (uint32_t)((use - 1) & 1), a.status)))
-                            break;
-                        uint8_t *dst = sRing + slot * SLOT_BYTES;
-                        mbar_arrive_expect_tx(&bs.kv_full[slot], SLOT_BYTES);
-                        const CUtensorMap *m = kv == 0 ? &tm_k : &tm_v;
-                        tma_load_4d(dst, m, &bs.kv_full[slot], 0, t * T, s.hk, s.b);
-                        tma_load_4d(dst + HALF_BYTES, m, &bs.kv_full[slot], 64, t * T, s.hk, s.b);
-                    }
-                    if (!ok) break;
-                }
-            }
-            // drain: wait for the last copies still in flight (consumed ones return at once)
-            const int64_t first = item > RING ? item - RING : 0;
-            for (int64_t n = first; n < item; ++n) drain_wait(&bs.kv_full[n % RING], (uint32_t)((n / RING) & 1));
-            drain_q(bs, split_tiles, q_loads);
-        }
+        if (lane == 0) produce_dense(bs, sRing, &tm_q, &tm_k, &tm_v, a, p, split_tiles, u_first, g0, g1, qload);
         __syncwarp();
     } else if (warp == WARP_MMA) {
         // ------------------------------------------------------------ MMA issuer
