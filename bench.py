@@ -40,16 +40,18 @@ FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes (read + written) per launch of the cache kernel from one ncu
 # capture, keyed by the sha256 of the kernel source it was taken on and the
-# workload; a changed kernel reports null. The capture and its command are
-# summarised in profiles/cache_attn_tc_llama3-8b-layer_ncu.md.
+# workload; a changed kernel reports null. The captures and their commands are
+# summarised in profiles/cache_attn_tc_llama3-8b-layer_ncu.md and
+# profiles/cache_attn_tc_sparse-hybrid_ncu.md.
 NCU_TRAFFIC = {
-    ("366fb684634d6190", "llama3-8b-layer-B4-L32k-N64-tree"): 541_603_840 + 8_358_656,
+    ("cdb83f410f5b09e1", "llama3-8b-layer-B4-L32k-N64-tree"): 540_644_864 + 8_498_432,
+    ("cdb83f410f5b09e1", "sparse-hybrid-B16-L32k-k2048-N8-chain"): 136_158_464 + 6_797_824,
 }
 
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for fn in ("attn_tc.cu", "sm100.cuh", "common.cuh"):
+    for fn in ("attn_tc.cu", "tc_pipe.cuh", "sm100.cuh", "common.cuh"):
         with open(os.path.join(ROOT, "speculative_decoding_verification_77_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
