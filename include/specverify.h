@@ -134,9 +134,9 @@ spec_status_t spec_verify_attn(const uint16_t *q, const uint16_t *k_cache,
  * 0 <= idx[b,j] < n and (j == 0 or idx[b,j] > idx[b,j-1]); -1 entries are
  * padding and are skipped silently; any other unused entry also records
  * SPEC_ERR_BAD_INPUT. The workspace size is
- * spec_verify_workspace_size(B, N, Hq, Hkv, d, budget). The cache rows of
- * every (b, h) must lie on a common grid of d-element rows: kv_stride_b,
- * kv_stride_h and kv_stride_t multiples of d.
+ * spec_verify_workspace_size(B, N, Hq, Hkv, d, budget). The cache strides
+ * follow the rule of spec_verify_attn (multiples of 8 elements): every
+ * gathered row starts on a 16-byte boundary.
  */
 spec_status_t spec_verify_attn_sparse(const uint16_t *q, const uint16_t *k_cache,
                                       const uint16_t *v_cache, int64_t kv_stride_b,

@@ -88,7 +88,6 @@ spec_status_t verify_common(const uint16_t *q, const uint16_t *k_cache, const ui
         return SPEC_ERR_INVALID_ARG;
     if (!(scale == scale)) return SPEC_ERR_INVALID_ARG;
     if (d != kHeadDim) return SPEC_ERR_UNSUPPORTED;
-    if (sparse && (sb % d || sh % d || st % d)) return SPEC_ERR_INVALID_ARG;
     if ((int64_t)B * N * Hq > (int64_t)1 << 31) return SPEC_ERR_INVALID_ARG;
     DeviceInfo dev;
     if (spec_status_t s = current_device(&dev)) return s;

@@ -274,11 +274,26 @@ def test_sparse_ragged_selection(ops):
     assert_attn_close(out, lse, ro, rl)
 
 
-@pytest.mark.parametrize("case", ["g3_warp_kernel", "token_major", "padding_runs", "row_groups", "one_tile"])
+def strided_cache(x, sb, sh, st):
+    """The cache tensor x [B, Hkv, L, d] copied into a device buffer with element strides (sb, sh, st, 1)."""
+    B, H, L, d = x.shape
+    flat = torch.zeros((B - 1) * sb + (H - 1) * sh + (L - 1) * st + d, dtype=x.dtype, device=dev())
+    view = torch.as_strided(flat, (B, H, L, d), (sb, sh, st, 1))
+    view.copy_(x.to(dev()))
+    return view
+
+
+@pytest.mark.parametrize("case", ["g3_warp_kernel", "token_major", "padding_runs", "row_groups", "one_tile",
+                                  "padded_rows", "padded_batch"])
 def test_sparse_paths(ops, case):
-    """Sparse verify on both cache kernels and on the index patterns each must mask."""
+    """Sparse verify on both cache kernels, on cache strides that are multiples of 8 but not of
+    d, and on the index patterns each must mask."""
     shapes = {"g3_warp_kernel": dict(B=2, N=7, Hq=12, Hkv=4, L=3000),  # G = 3: warp-level kernel
               "token_major": dict(B=2, N=5, Hq=8, Hkv=4, L=2500),
+              # token-major, token rows padded to 576 elements, batches shifted by 8 elements
+              "padded_rows": dict(B=3, N=5, Hq=8, Hkv=4, L=2500),
+              # head-major with batches shifted by 8 elements
+              "padded_batch": dict(B=3, N=5, Hq=8, Hkv=2, L=2500),
               "padding_runs": dict(B=2, N=5, Hq=8, Hkv=2, L=2500),
               "row_groups": dict(B=2, N=40, Hq=16, Hkv=2, L=2600),  # G*N = 320 rows: three row groups
               "one_tile": dict(B=1, N=3, Hq=4, Hkv=1, L=90)}[case]
@@ -301,6 +316,11 @@ def test_sparse_paths(ops, case):
     if case == "token_major":
         k = x["k_cache"].permute(0, 2, 1, 3).contiguous().to(dev()).permute(0, 2, 1, 3)
         v = x["v_cache"].permute(0, 2, 1, 3).contiguous().to(dev()).permute(0, 2, 1, 3)
+    if case == "padded_rows":
+        st = 4 * 128 + 64
+        k, v = (strided_cache(x[n], L * st + 8, 128, st) for n in ("k_cache", "v_cache"))
+    if case == "padded_batch":
+        k, v = (strided_cache(x[n], 2 * L * 128 + 8, L * 128, 128) for n in ("k_cache", "v_cache"))
     out, lse = ops.verify_attn_sparse(g["q"], k, v, g["k_draft"], g["v_draft"], g["parent"], idx.to(dev()),
                                       scale=x["scale"])
     ro, rl, st = oracle.attend(x["q"], x["k_cache"], x["v_cache"], x["k_draft"], x["v_draft"], x["parent"],
@@ -310,7 +330,7 @@ def test_sparse_paths(ops, case):
     assert_attn_close(out, lse, ro, rl)
 
 
-@pytest.mark.parametrize("slot", [0, 127, 128, 255, 1999])
+@pytest.mark.parametrize("slot", [0, 5, 70, 127, 128, 255, 1999])
 def test_sparse_needle_at_index_slot(ops, slot):
     """A key with logit ~ +30 behind index slot `slot`: o must be that key's V."""
     x = small(300 + slot, B=1, N=2, Hq=4, Hkv=2, L=9000)
