@@ -16,12 +16,6 @@ __device__ __forceinline__ float4 load_bf16x4(const __nv_bfloat16 *p) {
     return make_float4(fa.x, fa.y, fb.x, fb.y);
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
 // Reductions over the lanes that hold the same row j = lane % GB (lane bits >= log2 GB).
 template <int GB>
 __device__ __forceinline__ float group_max(float v) {
@@ -34,6 +28,46 @@ __device__ __forceinline__ float group_sum(float v) {
 #pragma unroll
     for (int o = 16; o >= GB; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
+}
+
+// Reduce-scatter across the warp: lane l holds V partial sums p[0..V) (V a
+// power of two, at most 32) and gets back the warp-wide sum of entry l % V. Each
+// halving step keeps the half of the entries whose index bit matches the lane's
+// and adds the partner's copy of that half; the lane bits above log2 V are then
+// summed with plain butterflies. 31 shuffles for V = 32 instead of 32 x 5.
+template <int V>
+__device__ __forceinline__ float reduce_scatter(float (&p)[V], int lane) {
+#pragma unroll
+    for (int h = V / 2; h >= 1; h >>= 1) {
+        const bool up = (lane & h) != 0;
+#pragma unroll
+        for (int t = 0; t < h; ++t) {
+            const float keep = up ? p[t + h] : p[t];
+            const float send = up ? p[t] : p[t + h];
+            p[t] = keep + __shfl_xor_sync(0xffffffffu, send, h);
+        }
+    }
+    float x = p[0];
+#pragma unroll
+    for (int o = 16; o >= V; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// GB consecutive floats of a warp's weight scratch (p aligned to GB floats).
+template <int GB>
+__device__ __forceinline__ void load_weights(const float *p, float (&w)[GB]) {
+    if constexpr (GB >= 4) {
+#pragma unroll
+        for (int c = 0; c < GB; c += 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(p + c);
+            w[c] = v.x; w[c + 1] = v.y; w[c + 2] = v.z; w[c + 3] = v.w;
+        }
+    } else if constexpr (GB == 2) {
+        const float2 v = *reinterpret_cast<const float2 *>(p);
+        w[0] = v.x; w[1] = v.y;
+    } else {
+        w[0] = p[0];
+    }
 }
 
 // Running log-sum-exp state of GB rows held by one warp (lane holds columns
@@ -83,10 +117,13 @@ struct RowsLse {
 // cache kernel's last CTAs; the wait for the partials comes after it. The
 // ancestor walk runs over the parent row staged in shared memory, and each
 // batch of draft K/V rows (shared by the GB heads) and of partials is loaded
-// in one go, so a warp makes a handful of round trips to memory.
+// in one go, so a warp makes a handful of round trips to memory. The logits of
+// a batch come out of one reduce-scatter, and the batch's weights reach every
+// lane through a 32-float scratch of the warp in shared memory.
 template <int GB>
 __global__ void __launch_bounds__(256) merge_tree_kernel(VerifyArgs a, SplitPlan p) {
     extern __shared__ int32_t parent_smem[];  // [warps per block][N]
+    __shared__ __align__(16) float w_smem[8][32];  // [warp][term * GB + head]: a batch's weights
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     const int nblk = a.G / GB;
@@ -105,6 +142,7 @@ __global__ void __launch_bounds__(256) merge_tree_kernel(VerifyArgs a, SplitPlan
     const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
 
     RowsLse<GB> st;
+    float *wsc = w_smem[threadIdx.x >> 5];
     // (b) speculative part: node i and its ancestors, TB at a time
     if (a.k_draft) {
         int32_t *ps = parent_smem + (threadIdx.x >> 5) * a.N;
@@ -138,26 +176,27 @@ __global__ void __launch_bounds__(256) merge_tree_kernel(VerifyArgs a, SplitPlan
                 kr[d] = d < nb ? load_bf16x4(kd + node * node_stride) : zero4;
                 vr[d] = d < nb ? load_bf16x4(vd + node * node_stride) : zero4;
             }
-            float logit = -INFINITY;  // lane d*GB + jj holds the logit of ancestor d for head jj
+            // lane d*GB + jj gets the logit of ancestor d for head jj (padding rows: -inf)
+            constexpr int V = TB * GB;
+            float pd[V];
 #pragma unroll
-            for (int d = 0; d < TB; ++d) {
-                if (d < nb) {
+            for (int d = 0; d < TB; ++d)
 #pragma unroll
-                    for (int jj = 0; jj < GB; ++jj) {
-                        const float dot = warp_sum(qv[jj].x * kr[d].x + qv[jj].y * kr[d].y +
-                                                   qv[jj].z * kr[d].z + qv[jj].w * kr[d].w) * a.scale;
-                        if (lane == d * GB + jj) logit = dot;
-                    }
-                }
-            }
+                for (int jj = 0; jj < GB; ++jj)
+                    pd[d * GB + jj] = qv[jj].x * kr[d].x + qv[jj].y * kr[d].y + qv[jj].z * kr[d].z + qv[jj].w * kr[d].w;
+            float logit = reduce_scatter<V>(pd, lane) * a.scale;
+            if (lane >= V || (lane & (V - 1)) / GB >= nb) logit = -INFINITY;
             const float e = st.begin_batch(logit, lane);
+            wsc[lane] = e;
+            __syncwarp();
 #pragma unroll
-            for (int d = 0; d < TB; ++d) {
-                if (d < nb) {
+            for (int d = 0; d < TB; ++d) {  // padding rows are zero with weight zero
+                float wd[GB];
+                load_weights<GB>(wsc + d * GB, wd);
 #pragma unroll
-                    for (int jj = 0; jj < GB; ++jj) st.add(jj, __shfl_sync(0xffffffffu, e, d * GB + jj), vr[d]);
-                }
+                for (int jj = 0; jj < GB; ++jj) st.add(jj, wd[jj], vr[d]);
             }
+            __syncwarp();  // the scratch is read before the next batch overwrites it
         }
     }
 
@@ -191,18 +230,23 @@ __global__ void __launch_bounds__(256) merge_tree_kernel(VerifyArgs a, SplitPlan
                 for (int jj = 0; jj < GB; ++jj)
                     x[uu][jj] = d0 + uu < nb ? *reinterpret_cast<const float4 *>(src + jj * kHeadDim) : zero4;
             }
-            if (d0 == 0) e = st.begin_batch(w, lane);  // after the first chunk's loads are issued
+            if (d0 == 0) {  // after the first chunk's loads are issued
+                e = st.begin_batch(w, lane);
+                wsc[lane] = e;
+                __syncwarp();
+            }
 #pragma unroll
             for (int uu = 0; uu < U; ++uu) {
                 if (d0 + uu < nb) {
+                    float wk[GB];
+                    load_weights<GB>(wsc + (d0 + uu) * GB, wk);
 #pragma unroll
-                    for (int jj = 0; jj < GB; ++jj) {
-                        const float ej = __shfl_sync(0xffffffffu, e, (d0 + uu) * GB + jj);
-                        if (ej != 0.f) st.add(jj, ej, x[uu][jj]);  // an empty partial may hold anything
-                    }
+                    for (int jj = 0; jj < GB; ++jj)
+                        if (wk[jj] != 0.f) st.add(jj, wk[jj], x[uu][jj]);  // an empty partial may hold anything
                 }
             }
         }
+        __syncwarp();  // the scratch is read before the next batch overwrites it
     }
 #pragma unroll
     for (int j = 0; j < GB; ++j) {
