@@ -309,8 +309,11 @@ cudaError_t merge_attributes() {
 }
 
 cudaError_t launch_merge_tree(const VerifyArgs &a, const SplitPlan &p, cudaStream_t s) {
-    // heads per warp: the largest of 8, 4, 2, 1 that divides G
-    const int gb = a.G % 8 == 0 ? 8 : a.G % 4 == 0 ? 4 : a.G % 2 == 0 ? 2 : 1;
+    // heads per warp: the largest of 8, 4, 2, 1 that divides G, halved while that leaves
+    // fewer than ~10 warps per SM to hide the latency of each warp's chain of loads
+    constexpr int64_t kMinWarps = 1536;
+    int gb = a.G % 8 == 0 ? 8 : a.G % 4 == 0 ? 4 : a.G % 2 == 0 ? 2 : 1;
+    while (gb > 1 && (int64_t)a.B * a.N * a.Hkv * (a.G / gb) < kMinWarps) gb >>= 1;
     const int64_t warps = (int64_t)a.B * a.N * a.Hkv * (a.G / gb);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((warps * 32 + 255) / 256));
