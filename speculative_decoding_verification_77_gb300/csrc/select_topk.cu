@@ -158,14 +158,20 @@ __device__ __forceinline__ bool candidate(const Chunk &c, int t, const uint32_t 
 }
 
 // k-th largest key (1 <= k <= candidates) among the candidates of the whole
-// sequence not marked in `excl`. Returns the key; *need = how many tokens with
-// exactly that key belong to the top k. Every CTA of the cluster returns the
-// same values. Uses acc buffers buf .. buf + 2.
+// sequence not marked in `excl`, resolved to the bits above *res_shift: the key
+// is returned with the bits below *res_shift zero, and *need = how many tokens
+// whose key agrees with it above *res_shift belong to the top k. The digit
+// passes stop early when the chosen bin holds exactly the keys still needed:
+// then all of them are in the top k whatever their lower bits. Every CTA of the
+// cluster returns the same values (they come from the cluster totals). Uses acc
+// buffers buf .. buf + 2.
 template <bool STAGED>
 __device__ uint32_t cluster_select(const float *score, const uint32_t *staged, const Chunk &c,
-                                   const uint32_t *excl, uint32_t k, SelectSmem &sm, int buf, uint32_t *need) {
+                                   const uint32_t *excl, uint32_t k, SelectSmem &sm, int buf, uint32_t *need,
+                                   int *res_shift) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t prefix = 0u, kr = k;
+    int last_shift = 0;
     for (int p = 0; p < kPassesPerTier; ++p) {
         const int shift = pass_shift(p);
         const uint32_t him = pass_hi_mask(p), dm = pass_digit_mask(p);
@@ -205,6 +211,7 @@ __device__ uint32_t cluster_select(const float *score, const uint32_t *staged, c
                 if (cum + cnt[j] >= kr) {
                     sm.bcast[1] = (uint32_t)(kBins - 1 - (4 * tid + j));
                     sm.bcast[2] = kr - cum;
+                    sm.bcast[3] = cnt[j] == kr - cum ? 1u : 0u;  // the whole bin is needed
                     break;
                 }
                 cum += cnt[j];
@@ -213,20 +220,27 @@ __device__ uint32_t cluster_select(const float *score, const uint32_t *staged, c
         __syncthreads();
         prefix |= sm.bcast[1] << shift;
         kr = sm.bcast[2];
+        const bool whole_bin = sm.bcast[3] != 0u;
         __syncthreads();
+        last_shift = shift;
+        if (whole_bin) break;  // the lower digits cannot change the set
     }
     *need = kr;
+    *res_shift = last_shift;
     return prefix;
 }
 
 // ORs into `bits` the top-k of the candidates not already in `excl`: keys
 // above `thr`, plus the first `need` tokens (by index, over the whole
-// sequence) whose key equals `thr`. `excl` may alias `bits`: each warp reads
-// and writes only its own words, a word's read before its write.
+// sequence) whose key equals `thr`, keys compared above bit `shift`. `excl`
+// may alias `bits`: each warp reads and writes only its own words, a word's
+// read before its write.
 template <bool STAGED>
 __device__ void mark_tier(const float *score, const uint32_t *staged, const Chunk &c, const uint32_t *excl,
-                          uint32_t *bits, uint32_t thr, uint32_t need, int ph, uint32_t rank, SelectSmem &sm) {
+                          uint32_t *bits, uint32_t thr, uint32_t need, int shift, int ph, uint32_t rank,
+                          SelectSmem &sm) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t thr_hi = thr >> shift;
     uint32_t weq = 0;
     for (int kk0 = 0; kk0 < c.rounds; kk0 += 4) {
         uint32_t key[4];
@@ -234,7 +248,7 @@ __device__ void mark_tier(const float *score, const uint32_t *staged, const Chun
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int t = c.seg0 + (kk0 + u) * 32 + lane;
-            const bool eq = candidate(c, t, excl, warp * c.rounds + kk0 + u, lane) && key[u] == thr;
+            const bool eq = candidate(c, t, excl, warp * c.rounds + kk0 + u, lane) && (key[u] >> shift) == thr_hi;
             weq += __popc(__ballot_sync(0xffffffffu, eq));
         }
     }
@@ -251,9 +265,10 @@ __device__ void mark_tier(const float *score, const uint32_t *staged, const Chun
             const int t = c.seg0 + (kk0 + u) * 32 + lane;
             const int word = warp * c.rounds + kk0 + u;
             const bool cand = candidate(c, t, excl, word, lane);
-            const bool eq = cand && key[u] == thr;
+            const uint32_t hi = key[u] >> shift;
+            const bool eq = cand && hi == thr_hi;
             const unsigned eqm = __ballot_sync(0xffffffffu, eq);
-            const bool take = cand && (key[u] > thr || (eq && (all_eq || run + __popc(eqm & lanemask_lt()) < need)));
+            const bool take = cand && (hi > thr_hi || (eq && (all_eq || run + __popc(eqm & lanemask_lt()) < need)));
             const unsigned w = __ballot_sync(0xffffffffu, take);
             if (lane == 0) bits[word] |= w;
             run += __popc(eqm);
@@ -324,16 +339,18 @@ select_topk_kernel(const float *__restrict__ draft, const float *__restrict__ ta
     if (m > 0) {  // tier 1: top-m by draft score
         if (STAGED) stage_keys(ds, staged, c, lane);
         uint32_t need;
-        const uint32_t thr = cluster_select<STAGED>(ds, staged, c, nullptr, (uint32_t)m, sm, buf, &need);
+        int shift;
+        const uint32_t thr = cluster_select<STAGED>(ds, staged, c, nullptr, (uint32_t)m, sm, buf, &need, &shift);
         buf += kPassesPerTier;
-        mark_tier<STAGED>(ds, staged, c, nullptr, bits, thr, need, 0, rank, sm);
+        mark_tier<STAGED>(ds, staged, c, nullptr, bits, thr, need, shift, 0, rank, sm);
         __syncthreads();
     }
     if (f > 0) {  // tier 2: fill by target score among the rest
         if (STAGED) stage_keys(ts, staged, c, lane);
         uint32_t need;
-        const uint32_t thr = cluster_select<STAGED>(ts, staged, c, bits, (uint32_t)f, sm, buf, &need);
-        mark_tier<STAGED>(ts, staged, c, bits, bits, thr, need, 1, rank, sm);
+        int shift;
+        const uint32_t thr = cluster_select<STAGED>(ts, staged, c, bits, (uint32_t)f, sm, buf, &need, &shift);
+        mark_tier<STAGED>(ts, staged, c, bits, bits, thr, need, shift, 1, rank, sm);
         __syncthreads();
     }
     // emission: sink u window u tiers, ascending
