@@ -11,6 +11,11 @@ Functions:
                    [cache ; draft tree] (Dustin "Workflow di Verifica";
                    LongSpec section 2.C tree mask)
   lse_merge(...)   log-sum-exp merge of two normalised parts (LongSpec section 2.C)
+  accept_commit(...) greedy acceptance of the draft tree and commit of the accepted
+                   draft K/V rows into the cache (Dustin "Workflow di Verifica",
+                   step 5; BASTION "Risultati Sperimentali": greedy decoding).
+                   Integer bookkeeping and row copies: written here in plain
+                   Python loops, for the small cases the tests use.
 
 Each returns (result..., status) where status 0 = ok, 5 = bad input seen.
 """
@@ -148,3 +153,87 @@ def lse_merge(o_a, lse_a, o_b, lse_b):
     if st == 1:
         raise ValueError("oracle_lse_merge: invalid argument")
     return out, lo
+
+
+def accept_commit(draft_token, parent, target_next, k_cache=None, v_cache=None, k_draft=None, v_draft=None,
+                  ctx_lens=None):
+    """Greedy (temperature 0) acceptance of a draft tree, then the cache commit.
+
+    The pages say that the target verifies the draft tokens and that the accepted
+    ones are appended to the cache while the rejected ones are dropped (Dustin
+    "Workflow di Verifica", steps 4-5), under greedy decoding (BASTION
+    "Risultati Sperimentali"). They do not spell the acceptance rule out; the
+    plainest reading, taken here:
+
+    * target_next[b, 0] is the target's greedy token after the last committed
+      token, target_next[b, 1 + i] its greedy token after draft node i;
+    * starting at the root (cur = -1), the next accepted node is the lowest-index
+      child c of cur (parent[c] == cur, c > cur) with draft_token[c] ==
+      target_next[b, cur + 1]; the walk stops when no child matches;
+    * the bonus token is target_next[b, last accepted node + 1];
+    * the accepted nodes' draft K/V rows (all KV heads) are copied, in path order,
+      to cache positions ctx_lens[b], ctx_lens[b] + 1, ..., and ctx_lens[b]
+      grows by the number copied.
+
+    A parent entry outside [-1, i) never makes node i a child (it is reported);
+    a context length outside [0, L] commits nothing, and rows past L are not
+    copied (both reported).
+
+    draft_token, parent: int [B, N]; target_next: int [B, N + 1]; caches
+    [B, Hkv, L, d] and drafts [B, N, Hkv, d] (any dtype, copied as they are);
+    ctx_lens int [B]. Returns (path [B, N] with -1 after the accepted nodes,
+    length [B], bonus [B], k_cache, v_cache, ctx_lens, status) with new arrays for
+    the caches and lengths (None when not given) and status 5 if anything was
+    reported, else 0.
+    """
+    tok = np.asarray(draft_token, dtype=np.int64)
+    par = np.asarray(parent, dtype=np.int64)
+    tn = np.asarray(target_next, dtype=np.int64)
+    B, N = tok.shape
+    if par.shape != (B, N) or tn.shape != (B, N + 1):
+        raise ValueError("accept_commit: shape mismatch")
+    path = np.full((B, N), -1, dtype=np.int64)
+    length = np.zeros(B, dtype=np.int64)
+    bonus = np.zeros(B, dtype=np.int64)
+    status = 0
+    for b in range(B):
+        for i in range(N):
+            if not (-1 <= par[b, i] < i):
+                status = 5
+        cur, n = -1, 0
+        while True:
+            want = tn[b, cur + 1]
+            nxt = -1
+            for c in range(cur + 1, N):
+                if par[b, c] == cur and tok[b, c] == want:
+                    nxt = c
+                    break
+            if nxt < 0:
+                break
+            path[b, n] = nxt
+            n += 1
+            cur = nxt
+        length[b] = n
+        bonus[b] = tn[b, cur + 1]
+    if k_cache is None:
+        return path, length, bonus, None, None, None, status
+    kc = np.array(k_cache, copy=True)
+    vc = np.array(v_cache, copy=True)
+    kd = np.asarray(k_draft)
+    vd = np.asarray(v_draft)
+    ctx = np.array(ctx_lens, dtype=np.int64, copy=True)
+    L = kc.shape[2]
+    for b in range(B):
+        c0 = int(ctx[b])
+        if not (0 <= c0 <= L):
+            status = 5
+            continue
+        fit = min(int(length[b]), L - c0)
+        if fit < length[b]:
+            status = 5
+        for j in range(fit):
+            node = path[b, j]
+            kc[b, :, c0 + j, :] = kd[b, node, :, :]
+            vc[b, :, c0 + j, :] = vd[b, node, :, :]
+        ctx[b] = c0 + fit
+    return path, length, bonus, kc, vc, ctx, status
