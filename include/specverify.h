@@ -160,6 +160,41 @@ spec_status_t spec_lse_merge(const float *o_a, const float *lse_a, const float *
                              void *stream);
 
 /* ------------------------------------------------------------------------ */
+/* Greedy acceptance of the draft tree and commit of the accepted draft K/V
+ * rows into the cache (Dustin "Workflow di Verifica", steps 4-5: accepted
+ * tokens join the cache, rejected ones are dropped; greedy decoding as in
+ * BASTION "Risultati Sperimentali").
+ *
+ * draft_token [B, N], parent [B, N] (as for spec_verify_attn) and target_next
+ * [B, N + 1]: int32, device. target_next[b, 0] is the target's greedy token
+ * after the last committed token, target_next[b, 1 + i] its greedy token after
+ * draft node i. From the root, the next accepted node is the lowest-index
+ * child c of the current node (parent[c] == current, c > current) whose
+ * draft_token equals target_next[b, current + 1]; the walk stops when none
+ * does.
+ * Outputs (device, int32): accept_path [B, N] = the accepted nodes in order,
+ * then -1; accept_len [B]; bonus_token [B] = target_next[b, last + 1].
+ * Commit (optional: pass k_cache, v_cache, k_draft, v_draft and ctx_lens all
+ * non-NULL, or all NULL): the caches [B, Hkv, L, d] bf16 (element strides as
+ * for spec_verify_attn, multiples of 8) receive, at positions ctx_lens[b],
+ * ctx_lens[b] + 1, ..., the rows k_draft/v_draft [B, N, Hkv, d] of the
+ * accepted nodes, and ctx_lens[b] (device, in/out) grows by the rows copied.
+ * Rows past L are not copied and a ctx_lens[b] outside [0, L] commits
+ * nothing; both, and a parent outside [-1, i), set SPEC_ERR_BAD_INPUT in
+ * *status (device int32, zeroed by the call first; may be NULL).
+ * Requires 1 <= N <= 4096, B >= 1, d == 128 (else SPEC_ERR_UNSUPPORTED) and
+ * 16-byte aligned caches and drafts. The caller owns every buffer; the call
+ * is asynchronous on `stream`.
+ */
+spec_status_t spec_accept_commit(const int32_t *draft_token, const int32_t *parent,
+                                 const int32_t *target_next, int B, int N, int32_t *accept_path,
+                                 int32_t *accept_len, int32_t *bonus_token, uint16_t *k_cache,
+                                 uint16_t *v_cache, int64_t kv_stride_b, int64_t kv_stride_h,
+                                 int64_t kv_stride_t, const uint16_t *k_draft,
+                                 const uint16_t *v_draft, int Hkv, int d, int L, int32_t *ctx_lens,
+                                 int32_t *status, void *stream);
+
+/* ------------------------------------------------------------------------ */
 /* Dense verification attention without a workspace (allocates nothing).
  *
  * The source pages have no counterpart to this entry point: it is a

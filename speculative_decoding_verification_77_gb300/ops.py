@@ -11,6 +11,7 @@ Names mirror the C ABI (include/specverify.h):
   verify_attn            -> spec_verify_attn
   verify_attn_sparse     -> spec_verify_attn_sparse
   lse_merge              -> spec_lse_merge
+  accept_commit          -> spec_accept_commit
   read_device_status     -> spec_read_device_status
 """
 
@@ -43,6 +44,7 @@ SIGNATURES = {
     "spec_lse_merge": (I, [P, P, P, P, P, P, I64, I, P]),
     "spec_verify_attn_noalloc": (I, [P, P, P, I64, I64, I64, P, P, P, I, I, I, I, I, I, P, F, P, P, P, P]),
     "spec_read_device_status": (I, [P, P]),
+    "spec_accept_commit": (I, [P, P, P, I, I, P, P, P, P, P, I64, I64, I64, P, P, I, I, I, P, P, P]),
     "spec_profile_events": (None, [P, P]),
     "spec_kernel_launches": (ctypes.c_uint64, []),
     "spec_last_cuda_error": (ctypes.c_char_p, []),
@@ -220,6 +222,54 @@ def lse_merge(o_a, lse_a, o_b, lse_b, out=None, lse_out=None):
     _check("spec_lse_merge", lib.spec_lse_merge(_ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), _ptr(out),
                                                 _ptr(lse_out), rows, d, _stream(o_a)))
     return out, lse_out
+
+
+def accept_commit(draft_token, parent, target_next, k_cache=None, v_cache=None, k_draft=None, v_draft=None,
+                  ctx_lens=None):
+    """Greedy acceptance of the draft tree, then (with the caches given) the commit of the
+    accepted draft K/V rows at [ctx_lens, ctx_lens + accepted), in place.
+
+    draft_token, parent int32 [B, N]; target_next int32 [B, N + 1]; caches bf16 [B, Hkv, L, d]
+    (d contiguous), drafts bf16 [B, N, Hkv, d] contiguous, ctx_lens int32 [B] (updated).
+    Returns (path int32 [B, N], length int32 [B], bonus int32 [B], status int32 [1]) on the
+    device; status holds SPEC_ERR_BAD_INPUT if a parent, a context length or the cache's
+    room was out of range.
+    """
+    lib = load_library()
+    _need(draft_token, torch.int32, "draft_token", 2)
+    _need(parent, torch.int32, "parent", 2)
+    _need(target_next, torch.int32, "target_next", 2)
+    for t, nm in ((draft_token, "draft_token"), (parent, "parent"), (target_next, "target_next")):
+        if not t.is_contiguous():
+            raise ValueError(f"{nm} must be contiguous")
+    B, N = draft_token.shape
+    if tuple(parent.shape) != (B, N) or tuple(target_next.shape) != (B, N + 1):
+        raise ValueError("shape mismatch")
+    dev = draft_token.device
+    path = torch.empty((B, N), dtype=torch.int32, device=dev)
+    length = torch.empty((B,), dtype=torch.int32, device=dev)
+    bonus = torch.empty((B,), dtype=torch.int32, device=dev)
+    status = torch.empty((1,), dtype=torch.int32, device=dev)
+    commit = k_cache is not None
+    Hkv = d = L = 0
+    sb = sh = st = 0
+    if commit:
+        _need(k_cache, torch.bfloat16, "k_cache", 4)
+        _need(v_cache, torch.bfloat16, "v_cache", 4)
+        _need(k_draft, torch.bfloat16, "k_draft", 4)
+        _need(v_draft, torch.bfloat16, "v_draft", 4)
+        _need(ctx_lens, torch.int32, "ctx_lens", 1)
+        if k_cache.stride() != v_cache.stride() or k_cache.shape != v_cache.shape or k_cache.stride(3) != 1:
+            raise ValueError("k_cache and v_cache must share shape and strides, with d contiguous")
+        if not (k_draft.is_contiguous() and v_draft.is_contiguous() and ctx_lens.is_contiguous()):
+            raise ValueError("k_draft, v_draft and ctx_lens must be contiguous")
+        _, Hkv, L, d = k_cache.shape
+        sb, sh, st = k_cache.stride(0), k_cache.stride(1), k_cache.stride(2)
+    _check("spec_accept_commit", lib.spec_accept_commit(
+        _ptr(draft_token), _ptr(parent), _ptr(target_next), B, N, _ptr(path), _ptr(length), _ptr(bonus),
+        _ptr(k_cache), _ptr(v_cache), sb, sh, st, _ptr(k_draft), _ptr(v_draft), Hkv, d, L, _ptr(ctx_lens),
+        _ptr(status), _stream(draft_token)))
+    return path, length, bonus, status
 
 
 def read_device_status(ws: torch.Tensor) -> int:

@@ -93,6 +93,20 @@ def test_select_rejects_bad_arguments_on_the_host(lib, over, code):
     assert lib.spec_select_topk(*a.values()) == code
 
 
+@pytest.mark.parametrize("over,code", [
+    (dict(tok=None), 1), (dict(N=0), 1), (dict(N=5000), 1), (dict(tok=18), 1),  # null, N out of range, misaligned
+    (dict(kc=16), 1),                              # commit arguments given only in part
+    (dict(kc=16, vc=16, kd=16, vd=16, ctx=16, d=64), 2),   # head_dim other than 128
+    (dict(kc=16, vc=16, kd=16, vd=16, ctx=16, st=100), 1),  # stride not a multiple of 8
+    (dict(kc=24, vc=16, kd=16, vd=16, ctx=16), 1),          # cache not 16-byte aligned
+])
+def test_accept_rejects_bad_arguments_on_the_host(lib, over, code):
+    a = dict(tok=16, par=16, tn=16, B=1, N=4, path=16, ln=16, bonus=16, kc=None, vc=None, sb=0, sh=0, st=128,
+             kd=None, vd=None, Hkv=1, d=128, L=8, ctx=None, status=None, stream=None)
+    a.update(over)
+    assert lib.spec_accept_commit(*a.values()) == code
+
+
 def test_merge_rejects_bad_arguments_on_the_host(lib):
     assert lib.spec_lse_merge(None, 4, 4, 4, 4, 4, 10, 128, None) == 1
     assert lib.spec_lse_merge(4, 4, 4, 4, 4, 4, -1, 128, None) == 1

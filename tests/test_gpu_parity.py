@@ -420,3 +420,76 @@ def test_workspace_too_small_is_rejected(ops):
     with pytest.raises(ops.SpecError) as e:
         ops.verify_attn(g["q"], g["k_cache"], g["v_cache"], g["k_draft"], g["v_draft"], g["parent"], ws=ws)
     assert e.value.code == 4
+
+
+# ---------------------------------------------------------------- acceptance and cache commit
+
+def accept_inputs(seed, B, N, Hkv, L, ctx, tree="random"):
+    """Random draft trees with small token ids (so that siblings share tokens) and the
+    target's tokens made to follow a random root path of each tree."""
+    rng = np.random.default_rng(seed)
+    if tree == "chain":
+        par = np.tile(np.arange(-1, N - 1, dtype=np.int32), (B, 1))
+    else:
+        par = np.stack([np.array([-1] + [int(rng.integers(max(-1, i - 9), i)) for i in range(1, N)], np.int32)
+                        for _ in range(B)])
+    tok = rng.integers(0, 4, (B, N)).astype(np.int32)
+    tn = rng.integers(0, 4, (B, N + 1)).astype(np.int32)
+    for b in range(B):
+        c = N - 1 if tree == "chain" else int(rng.integers(0, N))
+        while c >= 0:
+            tn[b, par[b, c] + 1] = tok[b, c]
+            c = par[b, c]
+    g = torch.Generator().manual_seed(seed)
+    kc = torch.randn((B, Hkv, L, 128), generator=g).to(torch.bfloat16)
+    vc = torch.randn((B, Hkv, L, 128), generator=g).to(torch.bfloat16)
+    kd = torch.randn((B, N, Hkv, 128), generator=g).to(torch.bfloat16)
+    vd = torch.randn((B, N, Hkv, 128), generator=g).to(torch.bfloat16)
+    return tok, par, tn, kc, vc, kd, vd, np.asarray(ctx, np.int32)
+
+
+@pytest.mark.parametrize("case", ["tree", "chain_n256", "n1", "room_runs_out", "bad_ctx", "bad_parent",
+                                  "no_commit", "token_major"])
+def test_accept_commit_matches_oracle(ops, case):
+    """Greedy acceptance and cache commit: path, length, bonus, caches and lengths bit-exact."""
+    B, N, Hkv, L = 4, 64, 8, 1024
+    tree = "random"
+    ctx = [0, 100, 517, 900]
+    if case == "chain_n256":
+        N, tree = 256, "chain"
+        ctx = [0, 3, 500, 768]
+    if case == "n1":
+        N = 1
+    if case == "room_runs_out":
+        ctx = [L - 1, L - 2, L, 10]
+    if case == "bad_ctx":
+        ctx = [-1, L + 5, 7, 8]
+    tok, par, tn, kc, vc, kd, vd, ctx = accept_inputs(11 + len(case), B, N, Hkv, L, ctx, tree)
+    if case == "bad_parent":
+        par[1, 5] = 5
+        par[2, 7] = -3
+    commit = case != "no_commit"
+    want = oracle.accept_commit(tok, par, tn, *((kc.view(torch.int16).numpy(), vc.view(torch.int16).numpy(),
+                                                 kd.view(torch.int16).numpy(), vd.view(torch.int16).numpy(), ctx)
+                                                if commit else ()))
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev())
+    if commit:
+        gk, gv = kc.to(dev()), vc.to(dev())
+        if case == "token_major":
+            gk = kc.permute(0, 2, 1, 3).contiguous().to(dev()).permute(0, 2, 1, 3)
+            gv = vc.permute(0, 2, 1, 3).contiguous().to(dev()).permute(0, 2, 1, 3)
+        gctx = d(ctx)
+        path, length, bonus, status = ops.accept_commit(d(tok), d(par), d(tn), gk, gv, kd.to(dev()), vd.to(dev()), gctx)
+    else:
+        path, length, bonus, status = ops.accept_commit(d(tok), d(par), d(tn))
+    torch.cuda.synchronize()
+    assert np.array_equal(path.cpu().numpy(), want[0])
+    assert np.array_equal(length.cpu().numpy(), want[1])
+    assert np.array_equal(bonus.cpu().numpy(), want[2])
+    assert int(status.item()) == want[6]
+    assert want[6] == (5 if case in ("room_runs_out", "bad_ctx", "bad_parent") else 0)
+    if commit:
+        assert np.array_equal(gctx.cpu().numpy(), want[5])
+        assert np.array_equal(gk.cpu().contiguous().view(torch.int16).numpy(), want[3])
+        assert np.array_equal(gv.cpu().contiguous().view(torch.int16).numpy(), want[4])
+        assert want[1].max() > 0  # the planted paths were accepted
