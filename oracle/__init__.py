@@ -11,6 +11,10 @@ Functions:
                    [cache ; draft tree] (Dustin "Workflow di Verifica";
                    LongSpec section 2.C tree mask)
   lse_merge(...)   log-sum-exp merge of two normalised parts (LongSpec section 2.C)
+  budget_plan(...) BASTION's hardware-aware budget controller: best-first tree
+                   growth from the drafter's marginals, the acceptance surrogate,
+                   the calibrated roofline latency and the speedup-based stop
+                   (BASTION "Metodologia" sections 1-3). Plain Python, fp64.
   accept_commit(...) greedy acceptance of the draft tree and commit of the accepted
                    draft K/V rows into the cache (Dustin "Workflow di Verifica",
                    step 5; BASTION "Risultati Sperimentali": greedy decoding).
@@ -237,3 +241,80 @@ def accept_commit(draft_token, parent, target_next, k_cache=None, v_cache=None, 
             vc[b, :, c0 + j, :] = vd[b, node, :, :]
         ctx[b] = c0 + fit
     return path, length, bonus, kc, vc, ctx, status
+
+
+def budget_plan(marginals, n_max, *, t_draft, l_ar, bytes0, bytes_per_node, flops_per_node, bw, peak, cal_n, cal_t):
+    """Tree size chosen by BASTION's online budget controller (BASTION "Metodologia").
+
+    Section 1 (path score): node i at depth d reached through candidates
+    c_1..c_d has rho(i) = prod_k q_k(c_k), q_k = marginals[k - 1].
+    Section 2 (surrogate, best-first expansion): A(T) = sum of rho over the
+    tree; the tree grows by repeatedly adding the frontier node with the largest
+    rho (a node's children are the candidates of the next position). Ties go to
+    the candidate that entered the frontier first (children enter in candidate
+    order).
+    Section 3 (controller): T_verify(N) comes from a roofline,
+    max((bytes0 + bytes_per_node N) / bw, flops_per_node N / peak), corrected as
+    a T_roof + c with (a, c) the least-squares fit to the measured samples
+    (cal_n, cal_t) (with fewer than two distinct roofline values: a = mean(t) /
+    mean(T_roof), c = 0). S(N) = A(T_N) l_ar / C(N) with C(N) = t_draft +
+    T_verify(N), the drafting cost being the same for every topology. The tree
+    grows one node at a time and the answer is the last N before S first
+    decreases (or the last N grown, at n_max or when no candidate is left).
+
+    Returns a dict: n (the chosen size), n_eval (sizes evaluated), parents,
+    depth, cand, rho (of the n_eval nodes grown), speedup (S(1..n_eval)), a, c.
+    """
+    q = np.asarray(marginals, dtype=np.float64)
+    K, C = q.shape
+    cal_n = np.asarray(cal_n, dtype=np.float64)
+    cal_t = np.asarray(cal_t, dtype=np.float64)
+
+    def t_roof(n):
+        return max((bytes0 + bytes_per_node * n) / bw, flops_per_node * n / peak)
+
+    x = np.array([t_roof(n) for n in cal_n])
+    if len(set(x.tolist())) < 2:
+        a, c = float(cal_t.mean() / x.mean()), 0.0
+    else:
+        xm, tm = x.mean(), cal_t.mean()
+        a = float(((x - xm) * (cal_t - tm)).sum() / ((x - xm) ** 2).sum())
+        c = float(tm - a * xm)
+
+    # frontier entries: [rho, order, parent, depth, candidate]
+    frontier = []
+    order = 0
+    for cc in range(C):
+        frontier.append([float(q[0, cc]), order, -1, 1, cc])
+        order += 1
+    parents, depth, cand, rho, speedup = [], [], [], [], []
+    surrogate = 0.0
+    n_star = 0
+    while len(parents) < n_max and frontier:
+        best = 0
+        for j in range(1, len(frontier)):
+            r, o = frontier[j][0], frontier[j][1]
+            if r > frontier[best][0] or (r == frontier[best][0] and o < frontier[best][1]):
+                best = j
+        r, _, par, dep, cc = frontier.pop(best)
+        node = len(parents)
+        parents.append(par)
+        depth.append(dep)
+        cand.append(cc)
+        rho.append(r)
+        if dep < K:
+            for c2 in range(C):
+                frontier.append([r * float(q[dep, c2]), order, node, dep + 1, c2])
+                order += 1
+        surrogate += r
+        n = node + 1
+        cost = t_draft + (a * t_roof(n) + c)
+        if not cost > 0:
+            raise ValueError("budget_plan: non-positive step cost")
+        speedup.append(surrogate * l_ar / cost)
+        if n >= 2 and speedup[-1] < speedup[-2]:
+            n_star = n - 1
+            break
+        n_star = n
+    return dict(n=n_star, n_eval=len(parents), parents=parents, depth=depth, cand=cand, rho=rho,
+                speedup=speedup, a=a, c=c)
