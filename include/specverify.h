@@ -160,6 +160,37 @@ spec_status_t spec_lse_merge(const float *o_a, const float *lse_a, const float *
                              void *stream);
 
 /* ------------------------------------------------------------------------ */
+/* Tree size for the next step from BASTION's hardware-aware budget controller
+ * ("Metodologia", sections 1-3). Runs on the host: every pointer is a host
+ * pointer and the call is synchronous.
+ *
+ * marginals [K, C] (row-major, values in [0, 1]): the drafter's probability of
+ * candidate c at tree depth k + 1. A node at depth d reached through
+ * candidates c_1..c_d scores rho = prod_k marginals[k - 1][c_k]; the tree grows
+ * best-first (largest rho next, ties to the candidate that entered the
+ * frontier first; a node's children enter in candidate order) up to n_max
+ * nodes. T_verify(N) = a T_roof(N) + c with T_roof(N) = max((bytes0 +
+ * bytes_per_node N) / bw, flops_per_node N / peak) (seconds, or any unit used
+ * throughout) and (a, c) the least-squares fit of cal_t on T_roof(cal_n) over
+ * the n_cal >= 1 measured samples (ratio of the means, c = 0, when the samples
+ * give fewer than two distinct T_roof). S(N) = (sum of the first N rho) l_ar /
+ * (t_draft + T_verify(N)); the tree grows one node at a time and *n_chosen is
+ * the last N before S first decreases (or the last N grown).
+ * Outputs (caller-owned host arrays of n_max entries): parents (-1 = root),
+ * depth (1-based), cand, rho of the *n_eval nodes grown; speedup[N - 1] =
+ * S(N) for N <= *n_eval; calib[0] = a, calib[1] = c.
+ * SPEC_ERR_INVALID_ARG for null pointers, K, C, n_max or n_cal below 1,
+ * non-finite inputs, bw or peak <= 0, marginals outside [0, 1], or a step
+ * cost t_draft + T_verify(N) <= 0.
+ */
+spec_status_t spec_budget_plan(const double *marginals, int K, int C, int n_max, double t_draft,
+                               double l_ar, double bytes0, double bytes_per_node,
+                               double flops_per_node, double bw, double peak, const double *cal_n,
+                               const double *cal_t, int n_cal, int32_t *parents, int32_t *depth,
+                               int32_t *cand, double *rho, double *speedup, double *calib,
+                               int32_t *n_chosen, int32_t *n_eval);
+
+/* ------------------------------------------------------------------------ */
 /* Greedy acceptance of the draft tree and commit of the accepted draft K/V
  * rows into the cache (Dustin "Workflow di Verifica", steps 4-5: accepted
  * tokens join the cache, rejected ones are dropped; greedy decoding as in

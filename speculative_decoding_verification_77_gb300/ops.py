@@ -12,6 +12,7 @@ Names mirror the C ABI (include/specverify.h):
   verify_attn_sparse     -> spec_verify_attn_sparse
   lse_merge              -> spec_lse_merge
   accept_commit          -> spec_accept_commit
+  budget_plan            -> spec_budget_plan (host)
   read_device_status     -> spec_read_device_status
 """
 
@@ -45,6 +46,8 @@ SIGNATURES = {
     "spec_verify_attn_noalloc": (I, [P, P, P, I64, I64, I64, P, P, P, I, I, I, I, I, I, P, F, P, P, P, P]),
     "spec_read_device_status": (I, [P, P]),
     "spec_accept_commit": (I, [P, P, P, I, I, P, P, P, P, P, I64, I64, I64, P, P, I, I, I, P, P, P]),
+    "spec_budget_plan": (I, [P, I, I, I, ctypes.c_double, ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                             ctypes.c_double, ctypes.c_double, ctypes.c_double, P, P, I, P, P, P, P, P, P, P, P]),
     "spec_profile_events": (None, [P, P]),
     "spec_kernel_launches": (ctypes.c_uint64, []),
     "spec_last_cuda_error": (ctypes.c_char_p, []),
@@ -270,6 +273,37 @@ def accept_commit(draft_token, parent, target_next, k_cache=None, v_cache=None, 
         _ptr(k_cache), _ptr(v_cache), sb, sh, st, _ptr(k_draft), _ptr(v_draft), Hkv, d, L, _ptr(ctx_lens),
         _ptr(status), _stream(draft_token)))
     return path, length, bonus, status
+
+
+def budget_plan(marginals, n_max: int, *, t_draft: float, l_ar: float, bytes0: float, bytes_per_node: float,
+                flops_per_node: float, bw: float, peak: float, cal_n, cal_t) -> dict:
+    """BASTION's budget controller on the host (see spec_budget_plan). marginals [K, C] array-like.
+    Returns dict(n, n_eval, parents, depth, cand, rho, speedup, a, c)."""
+    import numpy as np
+
+    lib = load_library()
+    q = np.ascontiguousarray(np.asarray(marginals, dtype=np.float64))
+    if q.ndim != 2:
+        raise ValueError("marginals must be [K, C]")
+    cn = np.ascontiguousarray(np.asarray(cal_n, dtype=np.float64).reshape(-1))
+    ct = np.ascontiguousarray(np.asarray(cal_t, dtype=np.float64).reshape(-1))
+    if cn.shape != ct.shape:
+        raise ValueError("cal_n and cal_t differ in length")
+    par = np.zeros(n_max, np.int32)
+    dep = np.zeros(n_max, np.int32)
+    cnd = np.zeros(n_max, np.int32)
+    rho = np.zeros(n_max, np.float64)
+    spd = np.zeros(n_max, np.float64)
+    cal = np.zeros(2, np.float64)
+    nc = np.zeros(1, np.int32)
+    ne = np.zeros(1, np.int32)
+    p = lambda a: ctypes.c_void_p(a.ctypes.data)
+    _check("spec_budget_plan", lib.spec_budget_plan(
+        p(q), q.shape[0], q.shape[1], n_max, t_draft, l_ar, bytes0, bytes_per_node, flops_per_node, bw, peak,
+        p(cn), p(ct), cn.shape[0], p(par), p(dep), p(cnd), p(rho), p(spd), p(cal), p(nc), p(ne)))
+    k = int(ne[0])
+    return dict(n=int(nc[0]), n_eval=k, parents=par[:k].tolist(), depth=dep[:k].tolist(), cand=cnd[:k].tolist(),
+                rho=rho[:k].tolist(), speedup=spd[:k].tolist(), a=float(cal[0]), c=float(cal[1]))
 
 
 def read_device_status(ws: torch.Tensor) -> int:
