@@ -11,6 +11,10 @@ Functions:
                    [cache ; draft tree] (Dustin "Workflow di Verifica";
                    LongSpec section 2.C tree mask)
   lse_merge(...)   log-sum-exp merge of two normalised parts (LongSpec section 2.C)
+  importance_scores(...) target-historical importance of every cache token: the
+                   final attention probabilities of the draft queries on the
+                   selected heads, summed (Dustin "Metodologia" sections 1-2).
+                   numpy, fp64.
   budget_plan(...) BASTION's hardware-aware budget controller: best-first tree
                    growth from the drafter's marginals, the acceptance surrogate,
                    the calibrated roofline latency and the speedup-based stop
@@ -318,3 +322,38 @@ def budget_plan(marginals, n_max, *, t_draft, l_ar, bytes0, bytes_per_node, flop
         n_star = n
     return dict(n=n_star, n_eval=len(parents), parents=parents, depth=depth, cand=cand, rho=rho,
                 speedup=speedup, a=a, c=c)
+
+
+def importance_scores(q, k_cache, lse, heads, *, scale: float, ctx_lens=None):
+    """Target-historical importance of each cache token (Dustin "Metodologia").
+
+    Section 1 fuses target-historical attention (the target's attention scores
+    from its forward passes) with the drafter's; section 2 restricts the scoring
+    to a few semantic retrieval heads found offline. The pages do not say how the
+    scores of several heads and queries combine; the plainest reading, taken
+    here: the score of cache token t of sequence b is the sum, over the listed
+    query heads h (a head listed twice counts twice) and the N draft queries i,
+    of the final attention probability of row (b, i, h) on t,
+    exp(scale q[b,i,h] . k[b, h // G, t] - lse[b,i,h]), with lse the row's
+    log-sum-exp over everything it attends (as spec_verify_attn returns it).
+    Tokens at or past ctx_lens[b] score 0, and so do rows with lse = -inf.
+
+    q [B, N, Hq, d], k_cache [B, Hkv, L, d], lse [B, N, Hq] (natural log),
+    heads: query-head indices. Returns fp64 [B, L].
+    """
+    qn = np.asarray(q, dtype=np.float64)
+    kc = np.asarray(k_cache, dtype=np.float64)
+    ln = np.asarray(lse, dtype=np.float64)
+    B, N, Hq, d = qn.shape
+    _, Hkv, L, _ = kc.shape
+    G = Hq // Hkv
+    ctx = np.full(B, L, dtype=np.int64) if ctx_lens is None else np.asarray(ctx_lens, dtype=np.int64)
+    out = np.zeros((B, L), dtype=np.float64)
+    for b in range(B):
+        n = int(min(max(ctx[b], 0), L))
+        for h in heads:
+            s = scale * (qn[b, :, h, :] @ kc[b, h // G, :n, :].T)  # [N, n]
+            row = ln[b, :, h][:, None]
+            p = np.where(np.isfinite(row), np.exp(s - np.where(np.isfinite(row), row, 0.0)), 0.0)
+            out[b, :n] += p.sum(axis=0)
+    return out
