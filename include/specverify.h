@@ -160,6 +160,29 @@ spec_status_t spec_lse_merge(const float *o_a, const float *lse_a, const float *
                              void *stream);
 
 /* ------------------------------------------------------------------------ */
+/* Target-historical importance of every cache token (Dustin "Metodologia",
+ * sections 1-2: the target's attention scores, estimated on a few semantic
+ * retrieval heads), the target score the next step's spec_select_topk reads.
+ *
+ * score[b * ld + t] = sum over the nh query heads heads[0..nh) (device int32;
+ * a head listed twice counts twice) and the N draft queries i of
+ * exp(scale q[b,i,h] . k[b, h / G, t] - lse[b,i,h]) for t < ctx_lens[b] (all L
+ * when ctx_lens is NULL), and 0 for ctx_lens[b] <= t < L. q and the cache as
+ * for spec_verify_attn; lse [B, N, Hq] fp32 as spec_verify_attn returns it
+ * (rows with lse = -inf add nothing). score: fp32 device, ld >= L. A head
+ * index outside [0, Hq) adds nothing and sets SPEC_ERR_BAD_INPUT in *status
+ * (device int32, zeroed by the call first; may be NULL).
+ * Requires d == 128 and N <= 512 (else SPEC_ERR_UNSUPPORTED), 1 <= B <= 65535,
+ * Hq % Hkv == 0, 16-byte aligned q and cache.
+ */
+spec_status_t spec_importance_scores(const uint16_t *q, const uint16_t *k_cache,
+                                     int64_t kv_stride_b, int64_t kv_stride_h,
+                                     int64_t kv_stride_t, const float *lse, const int32_t *heads,
+                                     int nh, int B, int N, int Hq, int Hkv, int d, int L,
+                                     const int32_t *ctx_lens, float scale, float *score, int64_t ld,
+                                     int32_t *status, void *stream);
+
+/* ------------------------------------------------------------------------ */
 /* Tree size for the next step from BASTION's hardware-aware budget controller
  * ("Metodologia", sections 1-3). Runs on the host: every pointer is a host
  * pointer and the call is synchronous.

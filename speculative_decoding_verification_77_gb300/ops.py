@@ -13,6 +13,7 @@ Names mirror the C ABI (include/specverify.h):
   lse_merge              -> spec_lse_merge
   accept_commit          -> spec_accept_commit
   budget_plan            -> spec_budget_plan (host)
+  importance_scores      -> spec_importance_scores
   read_device_status     -> spec_read_device_status
 """
 
@@ -46,6 +47,7 @@ SIGNATURES = {
     "spec_verify_attn_noalloc": (I, [P, P, P, I64, I64, I64, P, P, P, I, I, I, I, I, I, P, F, P, P, P, P]),
     "spec_read_device_status": (I, [P, P]),
     "spec_accept_commit": (I, [P, P, P, I, I, P, P, P, P, P, I64, I64, I64, P, P, I, I, I, P, P, P]),
+    "spec_importance_scores": (I, [P, P, I64, I64, I64, P, P, I, I, I, I, I, I, I, P, F, P, I64, P, P]),
     "spec_budget_plan": (I, [P, I, I, I, ctypes.c_double, ctypes.c_double, ctypes.c_double, ctypes.c_double,
                              ctypes.c_double, ctypes.c_double, ctypes.c_double, P, P, I, P, P, P, P, P, P, P, P]),
     "spec_profile_events": (None, [P, P]),
@@ -273,6 +275,36 @@ def accept_commit(draft_token, parent, target_next, k_cache=None, v_cache=None, 
         _ptr(k_cache), _ptr(v_cache), sb, sh, st, _ptr(k_draft), _ptr(v_draft), Hkv, d, L, _ptr(ctx_lens),
         _ptr(status), _stream(draft_token)))
     return path, length, bonus, status
+
+
+def importance_scores(q, k_cache, lse, heads, *, scale=None, ctx_lens=None, out=None):
+    """Target-historical importance of every cache token on the given query heads.
+
+    q [B,N,Hq,d] bf16, k_cache [B,Hkv,L,d] bf16 (d contiguous), lse fp32 [B,N,Hq] (from verify_attn),
+    heads int32 [nh] on the device. Returns (score fp32 [B, L], status int32 [1]).
+    """
+    import math
+
+    lib = load_library()
+    _need(q, torch.bfloat16, "q", 4)
+    _need(k_cache, torch.bfloat16, "k_cache", 4)
+    _need(lse, torch.float32, "lse", 3)
+    _need(heads, torch.int32, "heads", 1)
+    _need(ctx_lens, torch.int32, "ctx_lens", 1)
+    if not (q.is_contiguous() and lse.is_contiguous() and heads.is_contiguous()) or k_cache.stride(3) != 1:
+        raise ValueError("q, lse and heads must be contiguous and k_cache's d contiguous")
+    B, N, Hq, d = q.shape
+    _, Hkv, L, _ = k_cache.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, L), dtype=torch.float32, device=q.device)
+    status = torch.empty((1,), dtype=torch.int32, device=q.device)
+    _check("spec_importance_scores", lib.spec_importance_scores(
+        _ptr(q), _ptr(k_cache), k_cache.stride(0), k_cache.stride(1), k_cache.stride(2), _ptr(lse), _ptr(heads),
+        heads.numel(), B, N, Hq, Hkv, d, L, _ptr(ctx_lens), float(scale), _ptr(out), out.stride(0), _ptr(status),
+        _stream(q)))
+    return out, status
 
 
 def budget_plan(marginals, n_max: int, *, t_draft: float, l_ar: float, bytes0: float, bytes_per_node: float,

@@ -107,6 +107,17 @@ def test_accept_rejects_bad_arguments_on_the_host(lib, over, code):
     assert lib.spec_accept_commit(*a.values()) == code
 
 
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), 1), (dict(B=0), 1), (dict(B=70000), 1), (dict(Hq=3), 1), (dict(ld=10), 1),
+    (dict(st=100), 1), (dict(q=24), 1), (dict(d=64), 2), (dict(N=600), 2),
+])
+def test_importance_rejects_bad_arguments_on_the_host(lib, over, code):
+    a = dict(q=16, kc=16, sb=0, sh=0, st=128, lse=16, heads=16, nh=1, B=1, N=4, Hq=4, Hkv=2, d=128, L=64,
+             ctx=None, scale=ctypes.c_float(0.1), score=16, ld=64, status=None, stream=None)
+    a.update(over)
+    assert lib.spec_importance_scores(*a.values()) == code
+
+
 def test_merge_rejects_bad_arguments_on_the_host(lib):
     assert lib.spec_lse_merge(None, 4, 4, 4, 4, 4, 10, 128, None) == 1
     assert lib.spec_lse_merge(4, 4, 4, 4, 4, 4, -1, 128, None) == 1

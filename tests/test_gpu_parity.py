@@ -493,3 +493,36 @@ def test_accept_commit_matches_oracle(ops, case):
         assert np.array_equal(gk.cpu().contiguous().view(torch.int16).numpy(), want[3])
         assert np.array_equal(gv.cpu().contiguous().view(torch.int16).numpy(), want[4])
         assert want[1].max() > 0  # the planted paths were accepted
+
+
+# ---------------------------------------------------------------- importance scores
+
+@pytest.mark.parametrize("case", ["ragged", "repeated_heads_g8", "bad_head"])
+def test_importance_scores_match_oracle(ops, case):
+    """Target-historical scores on the listed heads. Both sides read the same lse: the attention
+    oracle's, rounded to fp32 (the dtype the library takes)."""
+    shapes = {"ragged": dict(B=2, N=8, Hq=8, Hkv=2, L=3000),
+              "repeated_heads_g8": dict(B=1, N=16, Hq=16, Hkv=2, L=1500),
+              "bad_head": dict(B=2, N=4, Hq=8, Hkv=2, L=700)}[case]
+    heads = {"ragged": [1, 6], "repeated_heads_g8": [0, 9, 9, 15], "bad_head": [2, 99]}[case]
+    x = small(91, depth=3, **shapes)
+    B, N, Hq, L = shapes["B"], shapes["N"], shapes["Hq"], shapes["L"]
+    ctx = np.array([L, 1234][:B] if case == "ragged" else [L] * B, np.int32)
+    _, lse64, st = oracle.attend(x["q"], x["k_cache"], x["v_cache"], x["k_draft"], x["v_draft"], x["parent"],
+                                 scale=x["scale"], ctx_lens=torch.from_numpy(ctx))
+    assert st == 0
+    lse32 = lse64.astype(np.float32).reshape(B, N, Hq)
+    valid = [h for h in heads if 0 <= h < Hq]
+    want = oracle.importance_scores(x["q"].float().numpy(), x["k_cache"].float().numpy(), lse32.astype(np.float64),
+                                    valid, scale=float(np.float32(x["scale"])), ctx_lens=ctx)
+    g = to_dev(x)
+    score, status = ops.importance_scores(g["q"], g["k_cache"], torch.from_numpy(lse32).to(dev()),
+                                          torch.tensor(heads, dtype=torch.int32, device=dev()), scale=x["scale"],
+                                          ctx_lens=torch.from_numpy(ctx).to(dev()))
+    torch.cuda.synchronize()
+    got = score.cpu().numpy()
+    assert int(status.item()) == (5 if case == "bad_head" else 0)
+    for b in range(B):
+        assert np.all(got[b, ctx[b]:] == 0.0)
+    assert np.allclose(got, want, rtol=1e-4, atol=1e-6), np.abs(got - want).max()
+    assert want.max() > 0
