@@ -13,6 +13,14 @@
  *   - "LongSpec", section 2.C (Hybrid Tree Attention): attention is split into
  *     the cache part (no mask) and the speculative part (tree mask), and the
  *     two are combined exactly with the log-sum-exp trick.
+ *   Around that path, the steps before and after it:
+ *   - Dustin, Metodologia sections 1-2: the target-historical importance of
+ *     each cache token on a few semantic retrieval heads (spec_importance_scores).
+ *   - Dustin, Workflow di Verifica step 5, under greedy decoding (BASTION,
+ *     Risultati Sperimentali): the accepted draft tokens join the cache
+ *     (spec_accept_commit).
+ *   - "BASTION", Metodologia sections 1-3: the hardware-aware choice of the
+ *     next tree's size (spec_budget_plan, on the host).
  *
  * Conventions shared by every entry point:
  *   - bf16 tensors are passed as `const uint16_t*` holding bf16 bit patterns.
@@ -34,7 +42,9 @@
  *     outside [0, L]) never trap: the offending entry is treated as masked,
  *     the rest of the result is computed, and SPEC_ERR_BAD_INPUT is recorded
  *     in the workspace's status word. Read it with spec_read_device_status().
- *     Each call clears the status word of its workspace first.
+ *     Each call clears the status word of its workspace first. The calls
+ *     without a workspace (spec_accept_commit, spec_importance_scores, the
+ *     no-alloc entry point) record it in a caller-given device word instead.
  *   - Layouts (row-major, innermost last):
  *       q        [B, N, Hq, d]           bf16   (query of draft node i, head h)
  *       k_cache, v_cache [B, Hkv, L, d]  bf16   element (b,h,t,c) at
