@@ -142,3 +142,26 @@ def test_product_does_not_use_the_oracle():
                     src = f.read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", src, re.M), fn
                 assert "spec_oracle" not in src and "oracle_attend" not in src, fn
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    """No CPU fallback anywhere: every tensor entry point of the binding rejects host tensors."""
+    import torch
+
+    from speculative_decoding_verification_77_gb300 import ops
+
+    bf = lambda *s: torch.zeros(s, dtype=torch.bfloat16)
+    i32 = lambda *s: torch.zeros(s, dtype=torch.int32)
+    f32 = lambda *s: torch.zeros(s, dtype=torch.float32)
+    calls = [
+        lambda: ops.select_topk(f32(1, 64), f32(1, 64), sink=1, window=1, top_m=2, budget=8),
+        lambda: ops.verify_attn(bf(1, 2, 4, 128), bf(1, 2, 16, 128), bf(1, 2, 16, 128)),
+        lambda: ops.verify_attn_sparse(bf(1, 2, 4, 128), bf(1, 2, 16, 128), bf(1, 2, 16, 128), None, None, None,
+                                       i32(1, 8)),
+        lambda: ops.lse_merge(f32(2, 128), f32(2), f32(2, 128), f32(2)),
+        lambda: ops.accept_commit(i32(1, 4), i32(1, 4), i32(1, 5)),
+        lambda: ops.importance_scores(bf(1, 2, 4, 128), bf(1, 2, 16, 128), f32(1, 2, 4), i32(1)),
+    ]
+    for call in calls:
+        with pytest.raises(ValueError, match="CUDA tensor"):
+            call()
