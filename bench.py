@@ -1,16 +1,22 @@
 """Benchmark: verification attention on one GB300 (or N replicas).
 
-One step = one spec_verify_attn call over the whole batch of the headline
-workload (Llama-3-8B-shaped layer: B=4, L=32768, 32 query / 8 KV heads,
-d=128, N=64-node random draft tree): the split-KV cache kernel plus the
-log-sum-exp merge fused with the tree-masked draft block.
+One step = one verification call over the whole batch of a workload. The
+contract line times the headline workload (Llama-3-8B-shaped layer: B=4,
+L=32768, 32 query / 8 KV heads, d=128, N=64-node random draft tree): one
+spec_verify_attn call, i.e. the split-KV cache kernel plus the log-sum-exp
+merge with the tree-masked draft block.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload C] [--impl native|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload C] [--extras LIST]
+                  [--impl native|reference]
 
 Prints one JSON line (rank 0). `value` is achieved HBM TB/s = algorithmic K/V
 bytes of all ranks / (max over ranks of the time per step); ms_per_step is the
-step latency. Inputs (512 MiB of K/V) exceed the 129 MB L2, so no flush is
-needed between steps. `--impl reference` times the CPU oracle (fp64, all host
+step latency. The headline's 512 MiB of K/V exceed the 129 MB L2, so no flush is
+needed between its steps. At N=1 the same run also times the other workloads
+(tiny dense, sparse hybrid, Qwen2.5-72B-shaped layer, the tree-size sweep) and
+reports them under "workloads", each with its own roofline fraction, oracle
+baseline and clock record; the tree-size sweep also calibrates BASTION's budget
+controller ("bastion"). `--impl reference` times the CPU oracle (fp64, all host
 cores) on a bounded sample of rows of the same workload.
 """
 
@@ -36,13 +42,13 @@ from speculative_decoding_verification_77_gb300 import workloads as W  # noqa: E
 
 METRIC = "verify-attention µs/step and achieved HBM TB/s (% of 8 TB/s) at B=4, L=32k"
 L2_BYTES = 129 * 1000 * 1000
-FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+SWEEP_N = (1, 4, 16, 64, 256)
 
 # DRAM bytes (read + written) per launch of the cache kernel from one ncu
-# capture, keyed by the sha256 of the kernel source it was taken on and the
-# workload; a changed kernel reports null. The captures and their commands are
-# summarised in profiles/cache_attn_tc_llama3-8b-layer_ncu.md and
-# profiles/cache_attn_tc_sparse-hybrid_ncu.md.
+# capture, keyed by the sha256 of the kernel sources it was taken on and the
+# workload; a changed kernel reports null.
 NCU_TRAFFIC = {
     ("cdb83f410f5b09e1", "llama3-8b-layer-B4-L32k-N64-tree"): 540_644_864 + 8_498_432,
     ("cdb83f410f5b09e1", "sparse-hybrid-B16-L32k-k2048-N8-chain"): 136_158_464 + 6_797_824,
@@ -61,9 +67,10 @@ def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
-            return json.load(f), "measured"
+            p = json.load(f)
+        return {k: float(p.get(k, FALLBACK_PEAKS[k])) for k in FALLBACK_PEAKS}, "measured"
     except (OSError, ValueError):
-        return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+        return dict(FALLBACK_PEAKS), "fallback"
 
 
 def dist_env():
@@ -84,6 +91,7 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.rows = None
 
     def start(self):
         try:
@@ -102,8 +110,6 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-
-    def summary(self, t0: float, t1: float):
         self.file.flush()
         self.file.seek(0)
         rows = []
@@ -117,20 +123,26 @@ class ClockSampler:
                 rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
             except ValueError:
                 continue
+        self.file.close()
         os.unlink(self.file.name)
+        self.rows = rows
+
+    def summary(self, t0: float, t1: float):
+        """Samples taken between t0 and t1 (wall clock; the whole run if none fall inside)."""
+        rows = self.rows or []
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-        inside = [r for r in rows if t0 - 1.0 <= r[0] <= t1 + 1.0]
-        window = "timed" if inside else "bench"
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
         use = inside or rows
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
-                "reasons": reasons, "samples": len(use), "window": window}
+                "reasons": reasons, "samples": len(use), "window": "timed" if inside else "bench",
+                "window_s": round(t1 - t0, 3)}
 
 
 # ---------------------------------------------------------------------------
-# native arm
+# oracle (CPU baseline)
 
 
 def oracle_select_seconds(x) -> float:
@@ -180,13 +192,213 @@ def oracle_baseline(x, rows_target_s: float = 10.0, max_rows: int | None = None)
         done += len(rows)
         if elapsed >= rows_target_s or done >= total_rows or (max_rows and done >= max_rows):
             break
-        n = min(total_rows, max(n, int(len(rows) * (rows_target_s - elapsed) / max(dt, 1e-3))))
+        n = min(total_rows - done, max(n, int(len(rows) * (rows_target_s - elapsed) / max(dt, 1e-3))))
+        if n <= 0:
+            break
     step_s = sel_s + elapsed / done * total_rows
     cores = len(os.sched_getaffinity(0))
     sel = f"selection of all {w.B} sequences {sel_s:.2f} s + " if w.sparse else ""
     return {"value": w.kv_bytes() / step_s / 1e12, "unit": "TB/s", "cores": cores, "kind": "oracle",
+            "s_per_step": round(step_s, 4),
             "sample": f"{sel}{done} of {total_rows} output rows (fp64, OpenMP over rows), {elapsed:.1f} s, "
                       f"extrapolated to one step: {step_s:.2f} s/step"}
+
+
+# ---------------------------------------------------------------------------
+# native arm
+
+
+class Case:
+    """One workload with its inputs resident on the device and its step functions."""
+
+    def __init__(self, w, dev, host_pinned: bool = False):
+        self.w = w
+        self.dev = dev
+        self.x = W.make_inputs(w)
+        names = ["q", "k_cache", "v_cache", "k_draft", "v_draft", "parent"]
+        if w.sparse:
+            names += ["draft_score", "target_score"]
+        self.names = names
+        self.host = {k: (self.x[k].pin_memory() if host_pinned else self.x[k]) for k in names}
+        self.g = {k: self.host[k].to(dev, non_blocking=True) for k in names}
+        torch.cuda.synchronize()
+        self.scale = self.x["scale"]
+        self.out = torch.empty((w.B, w.N, w.Hq, w.d), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((w.B, w.N, w.Hq), dtype=torch.float32, device=dev)
+        self.idx = torch.empty((w.B, max(w.budget, 1)), dtype=torch.int32, device=dev)
+        self.cnt = torch.empty((w.B,), dtype=torch.int32, device=dev)
+        # Inputs read per step smaller than 4x L2 (the sparse gather, the tiny case) get an L2
+        # flush before every step, outside the step's events; larger ones stream from HBM anyway.
+        self.flush = w.kv_bytes() < 4 * L2_BYTES
+        self.scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if self.flush else None
+        if w.sparse:  # the index set, for the attention-only timing
+            self.select(self.g)
+
+    def select(self, t):
+        from speculative_decoding_verification_77_gb300 import ops
+
+        w = self.w
+        ops.select_topk(t["draft_score"], t["target_score"], sink=w.sink, window=w.window, top_m=w.top_m,
+                        budget=w.budget, idx=self.idx, count=self.cnt)
+
+    def attend(self, t):
+        from speculative_decoding_verification_77_gb300 import ops
+
+        if self.w.sparse:
+            return ops.verify_attn_sparse(t["q"], t["k_cache"], t["v_cache"], t["k_draft"], t["v_draft"],
+                                          t["parent"], self.idx, scale=self.scale, out=self.out, lse=self.lse)
+        return ops.verify_attn(t["q"], t["k_cache"], t["v_cache"], t["k_draft"], t["v_draft"], t["parent"],
+                               scale=self.scale, out=self.out, lse=self.lse)
+
+    def step(self, t):
+        if self.w.sparse:
+            self.select(t)
+        return self.attend(t)
+
+    def do_flush(self, i):
+        if self.flush:
+            self.scratch.fill_(float(i))
+
+    def release(self):
+        for k in list(self.g):
+            del self.g[k]
+        self.scratch = None
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
+
+def ev():
+    return torch.cuda.Event(enable_timing=True)
+
+
+def time_loop(case, fn, stream, steps: int, min_seconds: float = 0.0):
+    """Per-call device times (ms) of fn(case.g), CUDA events on the launching stream, an L2
+    flush before each call when the case needs one. Runs at least `steps` calls and, with
+    min_seconds > 0, repeats batches of them until the loop has kept the GPU busy that long
+    (wall clock, flushes included), so that the clock sampler sees the load."""
+    times = []
+    start = time.time()
+    while True:
+        pairs = [(ev(), ev()) for _ in range(steps)]
+        for i, (a, b) in enumerate(pairs):
+            case.do_flush(i)
+            a.record(stream)
+            fn(case.g)
+            b.record(stream)
+        torch.cuda.synchronize()
+        times += [a.elapsed_time(b) for a, b in pairs]
+        if time.time() - start >= min_seconds:
+            return times
+
+
+def kernel_pass(case, stream, steps: int):
+    """Mean device time (ms) of the cache-attention kernel alone: CUDA events that the
+    library records around that launch on the launching stream. An event between the
+    cache kernel and the merge stops the merge from starting early (programmatic
+    dependent launch), so this pass is separate from the step timing."""
+    from speculative_decoding_verification_77_gb300 import ops
+
+    pairs = [(ev(), ev()) for _ in range(steps)]
+    for a, b in pairs:  # materialise the events before handing them to the library
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    for i, (a, b) in enumerate(pairs):
+        case.do_flush(i)
+        ops.profile_events(a, b)
+        case.step(case.g)
+    ops.profile_events(None, None)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in pairs) / steps
+
+
+def kernel_name(w):
+    if w.sparse:
+        return "cache_attn_tc<sparse> (tcgen05, cp.async row gather)"
+    return "cache_attn_tc (tcgen05 split-KV)"
+
+
+def roofline_entry(w, kernel_ms, peaks, peak_src):
+    """Roofline of the cache kernel: algorithmic K/V bytes and QK^T + PV flops per launch over
+    its mean duration, against the measured copy bandwidth and the sustained bf16 rate."""
+    kv, fl = w.kv_bytes(), w.flops()
+    gbs = kv / (kernel_ms * 1e-3) / 1e9
+    tfl = fl / (kernel_ms * 1e-3) / 1e12
+    t_hbm = kv / (peaks["hbm_gbs"] * 1e9)
+    t_tc = fl / (peaks["bf16_tflops_sustained"] * 1e12)
+    bound = "tensor" if t_tc > t_hbm else "hbm"
+    r = {"bound": bound, "kernel": kernel_name(w), "kernel_us": round(kernel_ms * 1e3, 2),
+         "achieved_gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
+         "frac_hbm_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+         "achieved_tflops": round(tfl, 1), "frac_tensor_sustained": round(tfl / peaks["bf16_tflops_sustained"], 4),
+         "frac_bound": round((t_tc if bound == "tensor" else t_hbm) / (kernel_ms * 1e-3), 4),
+         "traffic": NCU_TRAFFIC.get((kernel_source_hash(), w.name)),
+         "peaks": f"{peak_src}: hbm {peaks['hbm_gbs']} GB/s, bf16 sustained {peaks['bf16_tflops_sustained']} TFLOP/s"}
+    return r
+
+
+def time_extra(case, stream, args, peaks, peak_src, clocks_windows):
+    """Per-workload entry: step time (>= args.extra_seconds of device time), the cache kernel
+    alone, for sparse also the selection alone and the attention alone."""
+    w = case.w
+    for _ in range(3):
+        case.step(case.g)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    steps = time_loop(case, case.step, stream, args.steps, args.extra_seconds)
+    t1 = time.time()
+    kd_ms = kernel_pass(case, stream, args.steps)
+    step_ms = sum(steps) / len(steps)
+    kv = w.kv_bytes()
+    e = {"workload": w.name, "B": w.B, "L": w.L, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N,
+         "tree": w.tree + (f" depth<={w.depth_max}" if w.tree == "random" else ""),
+         "kv_bytes_per_step": kv, "flops_per_step": w.flops(),
+         "us_per_step": round(step_ms * 1e3, 2), "tb_per_s": round(kv / (step_ms * 1e-3) / 1e12, 4),
+         "frac_hbm_step": round(kv / (step_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+         "steps_timed": len(steps), "device_s_timed": round(sum(steps) * 1e-3, 3),
+         "l2": "flushed before every step (outside the events)" if case.flush else "inputs larger than L2, no flush",
+         "roofline": roofline_entry(w, kd_ms, peaks, peak_src)}
+    clocks_windows.append((e, t0, t1))
+    if w.sparse:
+        e.update(sink=w.sink, window=w.window, top_m=w.top_m, budget=w.budget,
+                 step="spec_select_topk + spec_verify_attn_sparse")
+        sel = time_loop(case, case.select, stream, args.steps, args.extra_seconds / 4)
+        att = time_loop(case, case.attend, stream, args.steps, args.extra_seconds / 4)
+        e["select_us"] = round(sum(sel) / len(sel) * 1e3, 2)
+        e["attention_us"] = round(sum(att) / len(att) * 1e3, 2)
+        e["attention_tb_per_s"] = round(kv / (sum(att) / len(att) * 1e-3) / 1e12, 4)
+    else:
+        e["step"] = "spec_verify_attn"
+    return e
+
+
+def bastion_calibration(sweep, marginals, peaks, args):
+    """BASTION's budget controller calibrated on the measured tree-size sweep: T_verify(N) =
+    a T_roof(N) + c fitted to the sweep's step times, then the best-first growth and the
+    speedup stop over the sweep workload's drafter marginals. Times in microseconds."""
+    from speculative_decoding_verification_77_gb300 import ops
+
+    w = W.workload(5, 1)
+    ns = [e["N"] for e in sweep]
+    ts = [e["us_per_step"] for e in sweep]
+    bytes0 = float(w.kv_bytes())
+    bytes_per_node = float(w.B * (w.Hq * w.d * 2 + 2 * w.Hkv * w.d * 2 + w.Hq * (w.d + 1) * 4))
+    flops_per_node = float(4 * w.B * w.Hq * w.L * w.d)
+    bw = peaks["hbm_gbs"] * 1e3  # bytes per microsecond
+    peak = peaks["bf16_tflops_sustained"] * 1e6  # flops per microsecond
+    l_ar = ts[ns.index(1)] if 1 in ns else min(ts)
+    t_draft = args.bastion_draft_ratio * l_ar
+    plan = ops.budget_plan(marginals, args.bastion_n_max, t_draft=t_draft, l_ar=l_ar, bytes0=bytes0,
+                           bytes_per_node=bytes_per_node, flops_per_node=flops_per_node, bw=bw, peak=peak,
+                           cal_n=ns, cal_t=ts)
+    n = plan["n"]
+    return {"cal_n": ns, "cal_t_us": ts, "a": round(plan["a"], 6), "c_us": round(plan["c"], 4),
+            "n_chosen": n, "speedup_at_chosen": round(plan["speedup"][n - 1], 4) if n >= 1 else None,
+            "surrogate_at_chosen": round(float(sum(plan["rho"][:n])), 4),
+            "n_eval": plan["n_eval"], "l_ar_us": round(l_ar, 3), "t_draft_us": round(t_draft, 3),
+            "bytes0": bytes0, "bytes_per_node": bytes_per_node, "flops_per_node": flops_per_node,
+            "marginals": "first sequence of the sweep workload (16 positions x 10 candidates, Dirichlet(0.3))",
+            "assumptions": f"L_AR = measured step at N=1; T_draft = {args.bastion_draft_ratio} x L_AR"}
 
 
 def run_native(args, ws_, rank, local):
@@ -194,91 +406,94 @@ def run_native(args, ws_, rank, local):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = W.workload(args.workload)
-    x = W.make_inputs(w)
-    names = ["q", "k_cache", "v_cache", "k_draft", "v_draft", "parent"]
-    if w.sparse:
-        names += ["draft_score", "target_score"]
-    host = {k: x[k].pin_memory() for k in names}
-    g = {k: host[k].to(dev, non_blocking=True) for k in names}
-    torch.cuda.synchronize()
-    scale = x["scale"]
-    out = torch.empty((w.B, w.N, w.Hq, w.d), dtype=torch.float32, device=dev)
-    lse = torch.empty((w.B, w.N, w.Hq), dtype=torch.float32, device=dev)
-    idx = torch.empty((w.B, max(w.budget, 1)), dtype=torch.int32, device=dev)
-    cnt = torch.empty((w.B,), dtype=torch.int32, device=dev)
+    peaks, peak_src = measured_peaks()
+    w = W.workload(args.workload, args.n)
+    case = Case(w, dev, host_pinned=not args.no_e2e)
     stream = torch.cuda.current_stream(dev)
 
-    def step(t):
-        if w.sparse:
-            ops.select_topk(t["draft_score"], t["target_score"], sink=w.sink, window=w.window, top_m=w.top_m,
-                            budget=w.budget, idx=idx, count=cnt)
-            return ops.verify_attn_sparse(t["q"], t["k_cache"], t["v_cache"], t["k_draft"], t["v_draft"],
-                                          t["parent"], idx, scale=scale, out=out, lse=lse)
-        return ops.verify_attn(t["q"], t["k_cache"], t["v_cache"], t["k_draft"], t["v_draft"], t["parent"],
-                               scale=scale, out=out, lse=lse)
-
-    # Inputs read per step smaller than 4x L2 (the sparse gather, the tiny case) get an L2 flush
-    # before every step, outside the step's events; larger ones stream from HBM anyway.
-    flush = w.kv_bytes() < 4 * L2_BYTES
-    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
-
     for _ in range(args.warmup):
-        step(g)
+        case.step(case.g)
     torch.cuda.synchronize()
-    ev = lambda: torch.cuda.Event(enable_timing=True)
-    kd_ev = [(ev(), ev()) for _ in range(args.steps)]
-    st_ev = [(ev(), ev()) for _ in range(args.steps)]
-    for a, b in kd_ev + st_ev:  # materialise the events before handing them to the library
-        a.record(stream)
-        b.record(stream)
     clocks = ClockSampler(local)
     clocks.start()
+    # untimed steps before the timed ones, so that the clock record brackets the timed region
+    t_pre = time.time()
+    while time.time() - t_pre < args.clock_window:
+        for i in range(20):
+            case.do_flush(i)
+            case.step(case.g)
+        torch.cuda.synchronize()
     barrier(ws_)
     torch.cuda.synchronize()
     launches0 = ops.kernel_launches()
-    t0 = time.time()
-    for i in range(args.steps):
-        if flush:
-            scratch.fill_(float(i))
-        st_ev[i][0].record(stream)
-        step(g)
-        st_ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    launches = ops.kernel_launches() - launches0
-    # The cache kernel's own duration, from a second pass of K steps with CUDA events that
-    # the library records around that launch. An event between the cache kernel and the
-    # merge stops the merge from starting early (programmatic dependent launch), so these
-    # events stay out of the pass that gives the step time.
-    for i in range(args.steps):
-        if flush:
-            scratch.fill_(float(i))
-        ops.profile_events(*kd_ev[i])
-        step(g)
-    ops.profile_events(None, None)
+    st_ev = [(ev(), ev()) for _ in range(args.steps)]
+    for i, (a, b) in enumerate(st_ev):
+        case.do_flush(i)
+        a.record(stream)
+        case.step(case.g)
+        b.record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
+    launches = ops.kernel_launches() - launches0
+    kd_ms = kernel_pass(case, stream, args.steps)
     barrier(ws_)
-    clocks.stop()
     ms = sum(a.elapsed_time(b) for a, b in st_ev) / args.steps
-    kd_ms = sum(a.elapsed_time(b) for a, b in kd_ev) / args.steps
     ms_max = allreduce_max(ws_, ms, dev)
 
-    # end to end through the public API: pinned host inputs -> device, verify, result -> host
-    if args.no_e2e:
-        e2e_ms = float("nan")
-        return finish(args, ws_, rank, w, ms, ms_max, kd_ms, launches, None, None, e2e_ms, clocks, t0, t1, x,
-                      flush)
-    dbuf = {k: torch.empty_like(g[k]) for k in names}
-    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    hlse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-    h2d = sum(host[k].numel() * host[k].element_size() for k in names)
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(case, stream, args, ws_, dev)
+    x = case.x
+    case.release()
+
+    extras = {}
+    bastion = None
+    windows = []
+    if ws_ == 1 and args.extras != "none":
+        wanted = [int(c) for c in args.extras.split(",")] if args.extras != "all" else [1, 2, 3, 4, 5]
+        sweep = []
+        marginals = None
+        for c in wanted:
+            for n in (SWEEP_N if c == 5 else (None,)):
+                wx = W.workload(c, n)
+                if wx.name == w.name:  # the headline itself: same run, reuse its numbers below
+                    continue
+                cx = Case(wx, dev)
+                e = time_extra(cx, stream, args, peaks, peak_src, windows)
+                if not args.no_cpu_baseline:
+                    e["cpu_baseline"] = oracle_baseline(cx.x, rows_target_s=args.extra_cpu_seconds)
+                if c == 5:
+                    sweep.append(e)
+                    if marginals is None:
+                        marginals = cx.x["trees"][0].marginals
+                extras[wx.name] = e
+                cx.release()
+                del cx
+        if sweep and marginals is not None:
+            head_e = None
+            if w.tree == "best_first" and w.name.startswith("tree-sweep"):
+                head_e = {"N": w.N, "us_per_step": round(ms * 1e3, 2)}
+            pts = sorted(sweep + ([head_e] if head_e else []), key=lambda e: e["N"])
+            bastion = bastion_calibration(pts, marginals, peaks, args)
+    clocks.stop()
+    for e, a, b in windows:
+        e["clocks"] = clocks.summary(a, b)
+    return finish(args, ws_, rank, w, ms, ms_max, kd_ms, launches, e2e, clocks, t_pre, t1, x, case.flush, peaks,
+                  peak_src, extras, bastion)
+
+
+def run_e2e(case, stream, args, ws_, dev):
+    """End to end through the public API: pinned host inputs -> device, verify, result -> host."""
+    dbuf = {k: torch.empty_like(case.g[k]) for k in case.names}
+    hout = torch.empty(case.out.shape, dtype=case.out.dtype, pin_memory=True)
+    hlse = torch.empty(case.lse.shape, dtype=case.lse.dtype, pin_memory=True)
+    h2d = sum(case.host[k].numel() * case.host[k].element_size() for k in case.names)
     d2h = hout.numel() * 4 + hlse.numel() * 4
 
     def e2e_step():
-        for k in names:
-            dbuf[k].copy_(host[k], non_blocking=True)
-        o, l_ = step(dbuf)
+        for k in case.names:
+            dbuf[k].copy_(case.host[k], non_blocking=True)
+        o, l_ = case.step(dbuf)
         hout.copy_(o, non_blocking=True)
         hlse.copy_(l_, non_blocking=True)
 
@@ -293,16 +508,19 @@ def run_native(args, ws_, rank, local):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = allreduce_max(ws_, e0.elapsed_time(e1) / args.steps, dev)
-    return finish(args, ws_, rank, w, ms, ms_max, kd_ms, launches, h2d, d2h, e2e_ms, clocks, t0, t1, x, flush)
+    del dbuf
+    return {"value": round(case.w.kv_bytes() / (e2e_ms * 1e-3) / 1e12, 4), "unit": "TB/s",
+            "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 
-def finish(args, ws_, rank, w, ms, ms_max, kd_ms, launches, h2d, d2h, e2e_ms, clocks, t0, t1, x, flush):
+def finish(args, ws_, rank, w, ms, ms_max, kd_ms, launches, e2e, clocks, t0, t1, x, flush, peaks, peak_src,
+           extras, bastion):
     if rank != 0:
         return None
-    peaks, peak_src = measured_peaks()
     kv = w.kv_bytes()
     achieved_gbs = kv / (kd_ms * 1e-3) / 1e9
     traffic = NCU_TRAFFIC.get((kernel_source_hash(), w.name))
+    rf = roofline_entry(w, kd_ms, peaks, peak_src)
     rec = {
         "metric": METRIC,
         "value": round(kv * ws_ / (ms_max * 1e-3) / 1e12, 4),
@@ -312,6 +530,8 @@ def finish(args, ws_, rank, w, ms, ms_max, kd_ms, launches, h2d, d2h, e2e_ms, cl
         "warmup": args.warmup,
         "ms_per_step": round(ms_max, 5),
         "us_per_step": round(ms_max * 1e3, 2),
+        "frac_hbm_step": round(kv / (ms_max * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+        "frac_hbm_step_nominal_8tbs": round(kv / (ms_max * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -319,19 +539,27 @@ def finish(args, ws_, rank, w, ms, ms_max, kd_ms, launches, h2d, d2h, e2e_ms, cl
         "data": "synthetic (seeded N(0,1) bf16 Q/K/V, " + ("softmax(4z) scores, " if w.sparse else "") +
                 f"{w.tree} draft tree)",
         "config": config_of(w, ws_, kv, flush),
-        "roofline": {"bound": "hbm", "kernel": kernel_name(w), "achieved": round(achieved_gbs, 1),
+        "roofline": {"bound": rf["bound"], "kernel": kernel_name(w), "achieved": round(achieved_gbs, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved_gbs / peaks["hbm_gbs"], 4),
+                     "frac_nominal_8tbs": round(achieved_gbs / NOMINAL_HBM_GBS, 4),
                      "peak_source": f"{peak_src} copy bandwidth", "traffic": traffic,
                      "kernel_ms": round(kd_ms, 5), "share_of_step": round(kd_ms / ms, 4),
+                     "achieved_tflops": rf["achieved_tflops"], "frac_tensor_sustained": rf["frac_tensor_sustained"],
                      "timing": "CUDA events around each cache-kernel launch, launching stream, second pass of K steps"},
         "gpu_launches": int(launches),
-        "e2e": None if h2d is None else {
-            "value": round(kv / (e2e_ms * 1e-3) / 1e12, 4), "unit": "TB/s", "ms_per_step": round(e2e_ms, 4),
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "e2e": e2e,
         "clocks": clocks.summary(t0, t1),
     }
+    if extras:
+        head = {"workload": w.name, "us_per_step": rec["us_per_step"], "tb_per_s": round(kv / (ms * 1e-3) / 1e12, 4),
+                "frac_hbm_step": rec["frac_hbm_step"], "roofline": rf, "note": "the contract line above"}
+        rec["workloads"] = {w.name: head, **extras}
+    if bastion is not None:
+        rec["bastion"] = bastion
     if ws_ == 1 and not args.no_cpu_baseline:  # the CPU baseline is taken on rank 0 at N=1 only
         rec["cpu_baseline"] = oracle_baseline(x, rows_target_s=args.cpu_seconds)
+        if extras:
+            rec["workloads"][w.name]["cpu_baseline"] = rec["cpu_baseline"]
     return rec
 
 
@@ -347,12 +575,6 @@ def config_of(w, ws_, kv, flush):
     else:
         c["step"] = "spec_verify_attn"
     return c
-
-
-def kernel_name(w):
-    if w.sparse:
-        return "cache_attn_tc<sparse> (tcgen05, cp.async row gather)"
-    return "cache_attn_tc (tcgen05 split-KV)"
 
 
 def barrier(ws_):
@@ -375,7 +597,7 @@ def allreduce_max(ws_, v: float, dev) -> float:
 def run_reference(args, ws_, rank):
     if rank != 0:
         return None
-    w = W.workload(args.workload)
+    w = W.workload(args.workload, args.n)
     x = W.make_inputs(w)
     total_rows = w.B * w.N * w.Hq
     per_step_rows = max(8, min(total_rows, args.ref_rows))
@@ -420,6 +642,15 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--n", type=int, default=None, help="draft-tree size of the tree-size sweep workload (5)")
+    ap.add_argument("--extras", default="all",
+                    help="other workloads timed in the same run at N=1: all, none, or a list like 1,3,4,5")
+    ap.add_argument("--extra-seconds", type=float, default=1.0, help="device time per extra workload")
+    ap.add_argument("--extra-cpu-seconds", type=float, default=2.0, help="oracle time per extra workload")
+    ap.add_argument("--clock-window", type=float, default=0.5,
+                    help="seconds of untimed steps before the timed ones, under the clock sampler")
+    ap.add_argument("--bastion-draft-ratio", type=float, default=1.0)
+    ap.add_argument("--bastion-n-max", type=int, default=512)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-rows", type=int, default=48)

@@ -266,11 +266,14 @@ spec_status_t spec_accept_commit(const int32_t *draft_token, const int32_t *pare
  * time - serving engines that reserve almost all of HBM for the KV cache at
  * start-up and allow no later allocation, or hosts that reach this library
  * from a plain C callback with no allocator - so they cannot pass the
- * workspace spec_verify_attn needs. This variant computes the same result with
- * the same kernels, but keeps its scratch (split partials and status word) in
- * a fixed 16 MiB array inside the library (every GPU that loads the library
- * holds it until the process exits). It calls no cudaMalloc, cudaFree or
- * other allocating routine.
+ * workspace spec_verify_attn needs. This variant computes the same result,
+ * within the parity tolerances (not bit for bit), through the warp-level
+ * tensor-core cache kernel (mma.sync) and the same merge kernel, rather than
+ * the tcgen05 cache kernel spec_verify_attn uses where the shape allows; its
+ * speed differs accordingly. It keeps its scratch (split partials and status
+ * word) in a fixed 16 MiB array inside the library, held by every GPU that has
+ * loaded the library's device code until the process exits. It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
  *
  * Arguments are those of spec_verify_attn without the workspace, plus
  * status_out: int32 device pointer that receives SPEC_OK or
@@ -280,7 +283,13 @@ spec_status_t spec_accept_commit(const int32_t *draft_token, const int32_t *pare
  * B=4, L=32768, Hq=32, Hkv=8, N=64 fits on a 152-SM GB300; B=8, Hq=64,
  * Hkv=8, N=32 does not.
  * The first call on each device looks up the array's device address (once,
- * with that device current); make that first call before any stream capture.
+ * with that device current). With lazy module loading (the CUDA default),
+ * that lookup is also when the 16 MiB array is placed in device memory, so
+ * make the first call on each device before reserving HBM for anything else,
+ * and before any stream capture. A failed lookup is remembered: later calls on
+ * that device return SPEC_ERR_CUDA.
+ * Problems whose split plan would number 2^31 tiles or more return
+ * SPEC_ERR_UNSUPPORTED, as spec_verify_attn does.
  * Every call on a device shares the one array: calls that overlap on the GPU
  * (different streams or threads, not ordered by the caller) race with each
  * other and must not be issued.

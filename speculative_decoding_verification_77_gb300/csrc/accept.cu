@@ -154,7 +154,10 @@ extern "C" spec_status_t spec_accept_commit(const int32_t *draft_token, const in
         if (d != kHeadDim) return SPEC_ERR_UNSUPPORTED;
     }
     const size_t smem = (size_t)(4 * N + 1) * sizeof(int32_t);
-    static const cudaError_t attr = kernel_attributes(accept_commit_kernel, (int)((4 * kAcceptMaxN + 1) * sizeof(int32_t)));
+    static PerDeviceOnce attr_once;
+    const cudaError_t attr = once_per_device(attr_once, [] {
+        return kernel_attributes(accept_commit_kernel, (int)((4 * kAcceptMaxN + 1) * sizeof(int32_t)));
+    });
     if (attr != cudaSuccess) return (spec_status_t)cuda_failure(attr);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (status) {

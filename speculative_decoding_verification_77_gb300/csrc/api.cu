@@ -14,7 +14,6 @@ thread_local cudaEvent_t g_prof_start = nullptr;
 thread_local cudaEvent_t g_prof_stop = nullptr;
 thread_local cudaError_t g_last_cuda_error = cudaSuccess;
 
-constexpr int kMaxDevices = 64;
 struct DeviceInfo {
     int ok;   // -1 unknown, 0 unsupported, 1 compute capability 10.3
     int sms;  // multiprocessor count

@@ -457,9 +457,11 @@ cudaError_t launch_cache_attn_tc(const VerifyArgs &a, const SplitPlan &p, cudaSt
     tp.M = a.G * a.N;
     tp.split_tiles = tp.M <= 128 ? 1 : 0;
     auto kern = sparse ? cache_attn_tc_kernel<true> : cache_attn_tc_kernel<false>;
-    static const cudaError_t attr_dense = kernel_attributes(cache_attn_tc_kernel<false>, SMEM_BYTES);
-    static const cudaError_t attr_sparse = kernel_attributes(cache_attn_tc_kernel<true>, SMEM_BYTES);
-    cudaError_t e = sparse ? attr_sparse : attr_dense;
+    static PerDeviceOnce attr_once;
+    cudaError_t e = once_per_device(attr_once, [] {
+        const cudaError_t r = kernel_attributes(cache_attn_tc_kernel<false>, SMEM_BYTES);
+        return r != cudaSuccess ? r : kernel_attributes(cache_attn_tc_kernel<true>, SMEM_BYTES);
+    });
     if (e != cudaSuccess) return e;
     if (ev0) cudaEventRecord(ev0, s);
     kern<<<p.ctas, THREADS, SMEM_BYTES, s>>>(a, p, tp, mq, mk, mv);

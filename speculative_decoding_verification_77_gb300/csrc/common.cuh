@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <mutex>
 #include <stdint.h>
 
 #include "../../include/specverify.h"
@@ -249,13 +250,32 @@ __device__ __forceinline__ int sparse_resolve(const VerifyArgs &a, IdxPair r, in
 int mma_rows_per_unit();
 int mma_tile_tokens();
 
-// Kernel attributes, set once per process (the launchers keep the result in a
-// function-local static): the dynamic shared memory a kernel may use beyond the
-// 48 KiB default.
+// Kernel attributes: the dynamic shared memory a kernel may use beyond the
+// 48 KiB default. The setting belongs to the current device's context, so the
+// launchers make it once per device, with that device current (once_per_device).
 template <class Kernel>
 cudaError_t kernel_attributes(Kernel kern, int dyn_smem) {
     if (dyn_smem <= 48 * 1024) return cudaSuccess;
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem);
+}
+
+// Per-device one-time set-up: f() runs once for each device index, the first time
+// a launcher runs with that device current, and its result is kept for that device.
+constexpr int kMaxDevices = 64;
+struct PerDeviceOnce {
+    std::once_flag once[kMaxDevices];
+    cudaError_t err[kMaxDevices] = {};
+};
+template <class F>
+cudaError_t once_per_device(PerDeviceOnce &st, F f) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return cudaErrorInvalidDevice;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::call_once(st.once[dev], [&] { st.err[dev] = f(); });
+    return st.err[dev];
 }
 
 // Records a failed CUDA call for spec_last_cuda_error() (this host thread) and

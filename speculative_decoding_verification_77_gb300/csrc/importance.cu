@@ -116,7 +116,9 @@ extern "C" spec_status_t spec_importance_scores(const uint16_t *q, const uint16_
     }
     if (L == 0) return SPEC_OK;
     const size_t smem = (size_t)N * 256 + (size_t)N * sizeof(float);
-    static const cudaError_t attr = kernel_attributes(importance_kernel, (int)(kImpMaxN * 256 + kImpMaxN * 4));
+    static PerDeviceOnce attr_once;
+    const cudaError_t attr = once_per_device(
+        attr_once, [] { return kernel_attributes(importance_kernel, (int)(kImpMaxN * 256 + kImpMaxN * 4)); });
     if (attr != cudaSuccess) return (spec_status_t)cuda_failure(attr);
     const dim3 grid((unsigned)((L + kImpThreads - 1) / kImpThreads), (unsigned)B);
     importance_kernel<<<grid, kImpThreads, smem, s>>>(

@@ -293,19 +293,19 @@ __global__ void __launch_bounds__(256) lse_merge2_kernel(const float *o_a, const
 
 }  // namespace
 
-// Attributes of the merge kernels, set once: shared memory for the largest N (8 warps x
-// 4096 parents) and the common carve-out.
+// Attributes of the merge kernels, set once per device: shared memory for the largest N
+// (8 warps x 4096 parents).
 cudaError_t merge_attributes() {
     constexpr int kMaxMergeSmem = 8 * 4096 * (int)sizeof(int32_t);
-    static const cudaError_t e = [] {
+    static PerDeviceOnce attr_once;
+    return once_per_device(attr_once, [] {
         cudaError_t r = kernel_attributes(merge_tree_kernel<8>, kMaxMergeSmem);
         if (r == cudaSuccess) r = kernel_attributes(merge_tree_kernel<4>, kMaxMergeSmem);
         if (r == cudaSuccess) r = kernel_attributes(merge_tree_kernel<2>, kMaxMergeSmem);
         if (r == cudaSuccess) r = kernel_attributes(merge_tree_kernel<1>, kMaxMergeSmem);
         if (r == cudaSuccess) r = kernel_attributes(lse_merge2_kernel, 0);
         return r;
-    }();
-    return e;
+    });
 }
 
 cudaError_t launch_merge_tree(const VerifyArgs &a, const SplitPlan &p, cudaStream_t s) {

@@ -8,8 +8,11 @@
 // plain C callback with no allocator of their own. This entry point keeps the
 // split-KV partials and the status word in a fixed, file-scope device array
 // instead, so it allocates nothing: no cudaMalloc, no cudaFree, no allocating
-// library call. The computation is the one spec_verify_attn does, through the
-// same cache kernel (warp-level tensor-core path) and the same merge kernel.
+// library call. It computes what spec_verify_attn computes, within the same
+// parity tolerances, but always through the warp-level tensor-core cache
+// kernel (mma.sync) and the merge kernel, not the tcgen05 cache kernel that
+// spec_verify_attn picks where the shape allows: the results agree within
+// tolerance, not bit for bit, and the speed differs.
 #include <mutex>
 
 #include "common.cuh"
@@ -24,14 +27,15 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;  // 16 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
 void *g_scratch_addr[kMaxDevices];
 cudaError_t g_scratch_err[kMaxDevices];
 std::once_flag g_scratch_once[kMaxDevices];
 
 // Device address of the scratch array on the current device (set up once per
 // device, with that device current). The array's name in host code is only a
-// host-side stand-in, so the kernels must be given this address instead.
+// host-side stand-in, so the kernels must be given this address instead. The
+// result of the first lookup is kept for the process, a failure included: a
+// device whose lookup failed keeps returning that error.
 cudaError_t scratch_address(int dev, void **out) {
     std::call_once(g_scratch_once[dev], [dev] {
         void *p = nullptr;
@@ -71,6 +75,9 @@ extern "C" spec_status_t spec_verify_attn_noalloc(
     if (!(scale == scale)) return SPEC_ERR_INVALID_ARG;
     if (d != kHeadDim) return SPEC_ERR_UNSUPPORTED;
     if ((int64_t)B * N * Hq > (int64_t)1 << 31) return SPEC_ERR_INVALID_ARG;
+    // the split plan numbers tiles in 32-bit arithmetic (the same guard as spec_verify_attn)
+    if ((int64_t)B * Hkv * (((int64_t)(Hq / Hkv) * N + 63) / 64) * ((int64_t)L / 64 + 1) >= ((int64_t)1 << 31))
+        return SPEC_ERR_UNSUPPORTED;
 
     int dev = 0, major = 0, minor = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices ||

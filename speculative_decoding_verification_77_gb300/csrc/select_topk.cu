@@ -390,15 +390,16 @@ cudaError_t launch_select_topk(const float *ds, const float *ts, int64_t ld, int
     const bool use_staged = staged <= 200 * 1024;
     const size_t smem = use_staged ? staged : base;
     auto kern = use_staged ? select_topk_kernel<true> : select_topk_kernel<false>;
-    // attributes for the largest shared memory either variant can need, set once
-    static const cudaError_t attr = [] {
+    // attributes for the largest shared memory either variant can need, set once per device
+    static PerDeviceOnce attr_once;
+    const cudaError_t attr = once_per_device(attr_once, [] {
         cudaError_t e = kernel_attributes(select_topk_kernel<true>, 200 * 1024);
         if (e == cudaSuccess) {
             const size_t Cmax = (size_t)chunk_tokens(kMaxL);
             e = kernel_attributes(select_topk_kernel<false>, (int)(sizeof(SelectSmem) + Cmax / 32 * sizeof(uint32_t)));
         }
         return e;
-    }();
+    });
     if (attr != cudaSuccess) return attr;
     kern<<<(unsigned)B * kCtas, kThreads, smem, s>>>(ds, ts, ld, L, ctx_lens, sink, window, top_m, budget, idx,
                                                      count, status);

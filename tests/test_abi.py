@@ -118,6 +118,20 @@ def test_importance_rejects_bad_arguments_on_the_host(lib, over, code):
     assert lib.spec_importance_scores(*a.values()) == code
 
 
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), 1), (dict(N=0), 1), (dict(Hq=3, Hkv=2), 1), (dict(st=100), 1), (dict(q=24), 1),
+    (dict(d=64), 2),
+    # 64 sequences x 1 KV head x (2^31 - 1) / 64 + 1 tiles = 2^31 tiles: beyond 32-bit tile numbering
+    (dict(B=64, L=2**31 - 1), 2),
+])
+def test_noalloc_rejects_bad_arguments_on_the_host(lib, over, code):
+    # fake, never-dereferenced addresses: every one of these checks returns before any CUDA call
+    a = dict(q=16, kc=16, vc=16, sb=0, sh=0, st=128, kd=None, vd=None, par=None, B=1, N=1, Hq=1, Hkv=1, d=128,
+             L=4, ctx=None, scale=ctypes.c_float(0.1), out=16, lse=16, status=None, stream=None)
+    a.update(over)
+    assert lib.spec_verify_attn_noalloc(*a.values()) == code
+
+
 def test_merge_rejects_bad_arguments_on_the_host(lib):
     assert lib.spec_lse_merge(None, 4, 4, 4, 4, 4, 10, 128, None) == 1
     assert lib.spec_lse_merge(4, 4, 4, 4, 4, 4, -1, 128, None) == 1

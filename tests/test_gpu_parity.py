@@ -84,10 +84,10 @@ def test_workload1_tiny_dense_all_rows(ops):
     run_dense(ops, x, to_dev(x))
 
 
-def test_workload2_llama_layer_sampled(ops):
+def test_workload2_llama_layer_all_rows(ops):
+    """The headline, every one of its 8,192 output rows against the oracle."""
     x = W.make_inputs(W.workload(2))
-    w = x["workload"]
-    run_dense(ops, x, to_dev(x), rows=sample_rows(w.B, w.N, w.Hq, 384))
+    run_dense(ops, x, to_dev(x))
 
 
 def test_workload3_sparse_hybrid(ops):
@@ -110,10 +110,30 @@ def test_workload3_sparse_hybrid(ops):
     assert_attn_close(out, lse, ro, rl, rows)
 
 
-def test_workload4_qwen_layer_sampled(ops):
+def unit_rows(w, per_half, seed):
+    """Rows covering every (b, h_kv) unit of a dense workload, per_half rows in each half of the
+    unit's rows (query heads of h_kv x draft nodes, node-major): the halves are the two softmax
+    pipes of the tensor-core kernel when a unit has more than 128 rows."""
+    rng = np.random.default_rng(seed)
+    G, half = w.G, max(1, w.N // 2)
+    rows = []
+    for b in range(w.B):
+        for hk in range(w.Hkv):
+            for lo, hi in ((0, half), (half, w.N)):
+                pick = rng.choice((hi - lo) * G, size=min(per_half, (hi - lo) * G), replace=False)
+                i, h = lo + pick // G, hk * G + pick % G
+                rows += ((b * w.N + i) * w.Hq + h).tolist()
+    return np.array(sorted(set(rows)), dtype=np.int64)
+
+
+def test_workload4_qwen_layer_every_unit(ops):
+    """Qwen2.5-72B-shaped layer (G = 8, L = 128k): 2,048 rows, 32 from every (b, h_kv) unit,
+    16 from each half of the unit's rows."""
     x = W.make_inputs(W.workload(4))
     w = x["workload"]
-    run_dense(ops, x, to_dev(x), rows=sample_rows(w.B, w.N, w.Hq, 96))
+    rows = unit_rows(w, 16, seed=4)
+    assert len(rows) == 2048 and len({(r // w.Hq // w.N, (r % w.Hq) // w.G) for r in rows}) == w.B * w.Hkv
+    run_dense(ops, x, to_dev(x), rows=rows)
 
 
 @pytest.mark.parametrize("N", [1, 4, 16, 64, 256])
