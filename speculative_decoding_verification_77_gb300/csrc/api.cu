@@ -188,7 +188,12 @@ spec_status_t spec_select_topk(const float *draft_score, const float *target_sco
     if (spec_status_t s = current_device(&dev)) return s;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint32_t *status = static_cast<uint32_t *>(workspace);
-    if (const cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s); e != cudaSuccess) return (spec_status_t)cuda_failure(e);
+    // the kernel writes the status word itself; with no sequence there is no kernel
+    if (B == 0) {
+        if (const cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s); e != cudaSuccess)
+            return (spec_status_t)cuda_failure(e);
+        return SPEC_OK;
+    }
     if (const cudaError_t e = launch_select_topk(draft_score, target_score, ld, B, L, ctx_lens, sink, window,
                                                  top_m, budget, idx, count, status, s);
         e != cudaSuccess)

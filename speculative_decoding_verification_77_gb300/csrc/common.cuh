@@ -30,6 +30,19 @@ __device__ __forceinline__ void flag_status(uint32_t *status, uint32_t code) {
     if (status) atomicMax(status, code);
 }
 
+// Status word of a selection call, written whole by block 0 of the grid (the other
+// blocks never write it, so no clearing memset has to come first): SPEC_ERR_BAD_INPUT
+// if a context length of the B sequences is outside [0, L], else SPEC_OK. Every
+// thread of block 0 calls it.
+__device__ __forceinline__ void select_status_block0(const int32_t *ctx_lens, int B, int L, uint32_t *status) {
+    if (blockIdx.x != 0) return;
+    int bad = 0;
+    if (ctx_lens)
+        for (int b = threadIdx.x; b < B; b += blockDim.x) bad |= ctx_lens[b] < 0 || ctx_lens[b] > L;
+    bad = __syncthreads_or(bad);
+    if (threadIdx.x == 0 && status) *status = bad ? (uint32_t)SPEC_ERR_BAD_INPUT : (uint32_t)SPEC_OK;
+}
+
 // ---------------------------------------------------------------------------
 // Split-KV work plan.
 //
@@ -292,6 +305,9 @@ cudaError_t launch_cache_attn_tc(const VerifyArgs &a, const SplitPlan &p, cudaSt
 cudaError_t launch_lse_merge2(const float *o_a, const float *lse_a, const float *o_b,
                               const float *lse_b, float *out, float *lse_out, int64_t rows, int d,
                               cudaStream_t s);
+bool launch_select_cluster_reg(const float *ds, const float *ts, int64_t ld, int B, int L, const int32_t *ctx_lens,
+                               int sink, int window, int top_m, int budget, int32_t *idx, int32_t *count,
+                               uint32_t *status, cudaStream_t s, cudaError_t *err);
 cudaError_t launch_select_topk(const float *ds, const float *ts, int64_t ld, int B, int L,
                                const int32_t *ctx_lens, int sink, int window, int top_m,
                                int budget, int32_t *idx, int32_t *count, uint32_t *status,

@@ -5,7 +5,8 @@
 // tokens by the draft-lookahead score, then the best remaining tokens by the
 // target-historical score. The result is emitted in ascending token order.
 //
-// One thread-block cluster of 8 CTAs per sequence; CTA r owns a contiguous
+// Contexts longer than 131072 tokens (shorter ones go to select_cl.cu): one
+// thread-block cluster of 8 CTAs per sequence; CTA r owns a contiguous
 // chunk of the context, and inside it warp w owns a contiguous segment that it
 // walks 32 tokens at a time (coalesced loads, one bitmap word per step). Each
 // tier is an exact radix select on a 32-bit order-preserving key of the fp32
@@ -298,13 +299,11 @@ select_topk_kernel(const float *__restrict__ draft, const float *__restrict__ ta
     const uint32_t rank = cluster_ctarank();
     const int b = blockIdx.x / kCtas;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    select_status_block0(ctx_lens, (int)(gridDim.x / kCtas), L, status);
     int n = L;
-    if (ctx_lens) {
+    if (ctx_lens) {  // a length outside [0, L] is clamped (and reported by block 0)
         n = ctx_lens[b];
-        if (n < 0 || n > L) {
-            if (rank == 0 && tid == 0) flag_status(status, SPEC_ERR_BAD_INPUT);
-            n = n < 0 ? 0 : L;
-        }
+        n = n < 0 ? 0 : (n > L ? L : n);
     }
     int32_t *out = idx + (int64_t)b * budget;
     if (budget >= n) {  // the whole context fits: verify in full (uniform over the cluster)
@@ -383,6 +382,11 @@ cudaError_t launch_select_topk(const float *ds, const float *ts, int64_t ld, int
                                int budget, int32_t *idx, int32_t *count, uint32_t *status,
                                cudaStream_t s) {
     if (B == 0) return cudaSuccess;
+    cudaError_t sub_err;
+    // up to 131072 tokens: a 4- or 8-CTA cluster per sequence with the keys in registers
+    if (launch_select_cluster_reg(ds, ts, ld, B, L, ctx_lens, sink, window, top_m, budget, idx, count, status, s,
+                                  &sub_err))
+        return sub_err;
     const size_t C = (size_t)chunk_tokens(L);
     const size_t base = sizeof(SelectSmem) + C / 32 * sizeof(uint32_t);
     const size_t staged = base + C * sizeof(uint32_t);

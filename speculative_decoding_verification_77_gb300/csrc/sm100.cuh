@@ -273,6 +273,12 @@ __device__ __forceinline__ uint32_t dsmem_ld(uint32_t addr) {
     asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
     return v;
 }
+// The two halves of cluster_sync(), for a split barrier: work between them overlaps
+// the wait for the other CTAs. Every arrive must be followed by a wait.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 // every thread of every CTA of the cluster; orders the shared-memory accesses
 // (local and remote) before it against those after it
 __device__ __forceinline__ void cluster_sync() {

@@ -371,13 +371,29 @@ def test_sparse_needle_at_index_slot(ops, slot):
     assert_attn_close(out, lse, ro, rl, rows)
 
 
-@pytest.mark.parametrize("case", ["ties", "special", "small_ctx", "big_top_m", "zero_top_m"])
+@pytest.mark.parametrize("case", ["ties", "special", "small_ctx", "big_top_m", "zero_top_m", "ties_32k",
+                                  "special_32k", "unaligned_rows_32k", "small_ctx_32k", "cluster_40k",
+                                  "cluster_ties_40k", "ties_12k", "cluster_100k", "staged_cluster_140k",
+                                  "staged_cluster_ties_140k"])
 def test_selection_cases_bit_exact(ops, case):
+    """Both selection kernels: a 4-CTA cluster per sequence with the keys in registers up to
+    64k tokens (one, two, four or eight quads per warp), 8 CTAs up to 128k, the cluster with
+    staged keys beyond."""
     B, L = 5, 5000
-    ds, ts = W.random_scores(B, L, seed=7, ties=3 if case == "ties" else 0)
+    if case.endswith("_32k"):
+        B, L = 3, 32768
+    if case.endswith("_40k"):
+        B, L = 3, 40000
+    if case.endswith("_12k"):
+        B, L = 4, 12000
+    if case.endswith("_100k"):
+        B, L = 2, 100000
+    if case.endswith("_140k"):
+        B, L = 2, 140000
+    ds, ts = W.random_scores(B, L, seed=7, ties=3 if "ties" in case else 0)
     kw = dict(sink=4, window=64, top_m=512, budget=1024)
     cl = None
-    if case == "special":
+    if case.startswith("special"):
         rng = np.random.default_rng(0)
         for arr in (ds, ts):
             pick = rng.choice(B * L, size=2000, replace=False)
@@ -385,11 +401,18 @@ def test_selection_cases_bit_exact(ops, case):
             arr.view(-1)[torch.from_numpy(pick)] = torch.from_numpy(rng.choice(vals, size=2000))
     if case == "small_ctx":
         cl = torch.tensor([5000, 1024, 1025, 68, 0], dtype=torch.int32)
+    if case == "small_ctx_32k":
+        cl = torch.tensor([32768, 1025, 20001], dtype=torch.int32)
     if case == "big_top_m":
         kw["top_m"] = 5000
     if case == "zero_top_m":
         kw["top_m"] = 0
-    idx, cnt = ops.select_topk(ds.to(dev()), ts.to(dev()), ctx_lens=None if cl is None else cl.to(dev()), **kw)
+    gds, gts = ds.to(dev()), ts.to(dev())
+    if case == "unaligned_rows_32k":  # row stride of 32771 floats: rows off 16-byte boundaries
+        pad = lambda t: torch.nn.functional.pad(t, (0, 3))[:, :L]
+        gds, gts = pad(gds), pad(gts)
+        assert gds.stride(0) == L + 3
+    idx, cnt = ops.select_topk(gds, gts, ctx_lens=None if cl is None else cl.to(dev()), **kw)
     ridx, rcnt, _ = oracle.select(ds, ts, ctx_lens=cl, **kw)
     assert np.array_equal(idx.cpu().numpy(), ridx)
     assert np.array_equal(cnt.cpu().numpy(), rcnt)
@@ -422,6 +445,19 @@ def test_bad_inputs_set_the_status_word(ops):
     ops.verify_attn(g["q"], g["k_cache"], g["v_cache"], g["k_draft"], g["v_draft"], g["parent"],
                     scale=x["scale"], ws=ws)
     assert ops.read_device_status(ws) == 0
+    # selection: a context length outside [0, L] is clamped and reported, on both selection
+    # kernels (registers up to 128k tokens, staged keys beyond); a clean call reports nothing
+    for L in (3000, 140000):
+        ds, ts = W.random_scores(3, L, seed=L)
+        kw = dict(sink=4, window=16, top_m=64, budget=256)
+        sws = torch.full((256,), 255, dtype=torch.uint8, device=dev())
+        cl = torch.tensor([L, -5, L + 9], dtype=torch.int32)
+        idx, cnt = ops.select_topk(ds.to(dev()), ts.to(dev()), ctx_lens=cl.to(dev()), ws=sws, **kw)
+        assert ops.read_device_status(sws) == 5
+        ridx, rcnt, st = oracle.select(ds, ts, ctx_lens=cl, **kw)
+        assert st == 5 and np.array_equal(idx.cpu().numpy(), ridx) and np.array_equal(cnt.cpu().numpy(), rcnt)
+        ops.select_topk(ds.to(dev()), ts.to(dev()), ws=sws, **kw)
+        assert ops.read_device_status(sws) == 0
 
 
 def test_native_kernels_ran(ops):
