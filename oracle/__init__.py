@@ -10,6 +10,9 @@ Functions:
   attend(...)      monolithic fp64 softmax attention with an explicit mask over
                    [cache ; draft tree] (Dustin "Workflow di Verifica";
                    LongSpec section 2.C tree mask)
+  attend_paged(...) attend() over a paged cache: the same cache in fixed-size blocks
+                   of a pool, found through a per-sequence block table (a layout the
+                   pages do not use)
   lse_merge(...)   log-sum-exp merge of two normalised parts (LongSpec section 2.C)
   importance_scores(...) target-historical importance of every cache token: the
                    final attention probabilities of the draft queries on the
@@ -73,6 +76,13 @@ def load_library(path: str):
                                   ctypes.c_int, ctypes.c_int, P, ctypes.c_float,
                                   ctypes.c_int64, ctypes.c_int64, P, ctypes.c_int64, P, P]
     lib.oracle_attend.restype = ctypes.c_int
+    lib.oracle_attend_paged.argtypes = [P, P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                        P, ctypes.c_int64, ctypes.c_int, ctypes.c_int64,
+                                        P, P, P, P, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_int, P, ctypes.c_float,
+                                        P, ctypes.c_int64, P, P]
+    lib.oracle_attend_paged.restype = ctypes.c_int
     lib.oracle_lse_merge.argtypes = [P, P, P, P, ctypes.c_int64, ctypes.c_int, P, P]
     lib.oracle_lse_merge.restype = ctypes.c_int
     return lib
@@ -142,6 +152,47 @@ def attend(q, k_cache, v_cache, k_draft, v_draft, parent, *, scale: float, ctx_l
                                t0, t1, _ptr(rows), rows.shape[0], _ptr(out), _ptr(lse))
     if st == 1:
         raise ValueError("oracle_attend: invalid argument")
+    return out, lse, st
+
+
+def attend_paged(q, k_pool, v_pool, k_draft, v_draft, parent, block_table, *, L: int, scale: float,
+                 ctx_lens=None, idx=None, rows=None, num_blocks=None):
+    """attend() over a paged cache (a layout the pages do not use): the cache of
+    sequence b is stored in fixed-size blocks of a pool, token t being row
+    t % block_size of pool block block_table[b, t // block_size]. A block entry
+    outside [0, num_blocks) hides its tokens and is reported (status 5).
+
+    k_pool/v_pool [num_blocks, Hkv, block_size, d] bf16 (copied contiguous);
+    block_table int32 [B, max_blocks] with max_blocks >= ceil(L / block_size); num_blocks
+    (default: all the pool's blocks) is how many blocks entries may name.
+    Returns (out float64 [n_rows, d], lse float64 [n_rows], status).
+    """
+    qn = _np(q, np.uint16)
+    B, N, Hq, d = qn.shape
+    kp = _np(k_pool, np.uint16)
+    vp = _np(v_pool, np.uint16)
+    nblk, Hkv, bs, _ = kp.shape
+    if num_blocks is not None:
+        assert 0 <= num_blocks <= nblk
+        nblk = num_blocks
+    kd = _np(k_draft, np.uint16)
+    vd = _np(v_draft, np.uint16)
+    par = _np(parent, np.int32)
+    tab = _np(block_table, np.int32)
+    ix = _np(idx, np.int32)
+    budget = 0 if ix is None else ix.shape[1]
+    cl = _np(ctx_lens, np.int32)
+    if rows is None:
+        rows = np.arange(B * N * Hq, dtype=np.int64)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty((rows.shape[0], d), dtype=np.float64)
+    lse = np.empty((rows.shape[0],), dtype=np.float64)
+    st = _load().oracle_attend_paged(_ptr(qn), _ptr(kp), _ptr(vp), Hkv * bs * d, bs * d, d, _ptr(tab),
+                                     tab.shape[1], bs, nblk, _ptr(kd), _ptr(vd), _ptr(par), _ptr(ix), budget,
+                                     B, N, Hq, Hkv, d, L, _ptr(cl), ctypes.c_float(scale), _ptr(rows),
+                                     rows.shape[0], _ptr(out), _ptr(lse))
+    if st == 1:
+        raise ValueError("oracle_attend_paged: invalid argument")
     return out, lse, st
 
 

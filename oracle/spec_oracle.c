@@ -29,6 +29,11 @@
  *   oracle_lse_merge  the log-sum-exp combination of two normalised partial
  *                   attentions (LongSpec section 2.C, "Aggregazione").
  *
+ *   oracle_attend_paged  oracle_attend over a paged cache (not on the pages: the
+ *                   same cache stored in fixed-size blocks of a pool, found through
+ *                   a per-sequence block table). A block entry outside the pool
+ *                   hides its tokens and is reported as bad input.
+ *
  * Readings where the pages are silent (also listed in the design notes):
  *   - score comparison: larger is better; -0 == +0; NaN ranks below every
  *     number (including -inf) and NaNs tie; ties go to the lower index.
@@ -160,12 +165,37 @@ int oracle_select(const float *draft_score, const float *target_score, int64_t l
 /* ------------------------------------------------------------------------ */
 /* attention                                                                 */
 
-int oracle_attend(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
-                  int64_t stride_b, int64_t stride_h, int64_t stride_t,
-                  const uint16_t *k_draft, const uint16_t *v_draft, const int32_t *parent,
-                  const int32_t *idx, int budget, int B, int N, int Hq, int Hkv, int d, int L,
-                  const int32_t *ctx_lens, float scale, int64_t cache_begin, int64_t cache_end,
-                  const int64_t *rows, int64_t n_rows, double *out, double *lse)
+/* Where the cache rows live. Contiguous (table == NULL): element (b, h, t, c) at
+   b*sb + h*sh + t*st + c. Paged (a layout the pages do not use; the same cache stored
+   in blocks of a pool): token t of sequence b is row t % block_size of pool block
+   table[b*table_ld + t / block_size], element (blk, h, o, c) at blk*sb + h*sh + o*st + c. */
+typedef struct {
+    int64_t sb, sh, st;
+    const int32_t *table;
+    int64_t table_ld;
+    int block_size;
+    int64_t num_blocks;
+} cache_layout;
+
+/* Element offset of the row of token t (sequence b, KV head hk); 0 when the row does not
+   exist (a block entry outside [0, num_blocks)), else 1. */
+static int cache_row(const cache_layout *cl, int b, int hk, int64_t t, int64_t *off)
+{
+    if (!cl->table) {
+        *off = b * cl->sb + hk * cl->sh + t * cl->st;
+        return 1;
+    }
+    int64_t blk = cl->table[b * cl->table_ld + t / cl->block_size];
+    if (blk < 0 || blk >= cl->num_blocks) return 0;
+    *off = blk * cl->sb + hk * cl->sh + (t % cl->block_size) * cl->st;
+    return 1;
+}
+
+static int attend_core(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                       const cache_layout *cl, const uint16_t *k_draft, const uint16_t *v_draft,
+                       const int32_t *parent, const int32_t *idx, int budget, int B, int N, int Hq,
+                       int Hkv, int d, int L, const int32_t *ctx_lens, float scale, int64_t cache_begin,
+                       int64_t cache_end, const int64_t *rows, int64_t n_rows, double *out, double *lse)
 {
     if (B < 1 || N < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || d < 1 || L < 0 || !q || !out ||
         !lse || !rows || (L > 0 && (!k_cache || !v_cache)) || (idx && budget < 0) ||
@@ -193,7 +223,7 @@ int oracle_attend(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_
         int64_t ncache_cand = idx ? budget : n;
         int64_t nkeys = ncache_cand + N;
         unsigned char *visible = (unsigned char *)calloc((size_t)(nkeys > 0 ? nkeys : 1), 1);
-        int64_t *token = (int64_t *)malloc(sizeof(int64_t) * (size_t)(ncache_cand > 0 ? ncache_cand : 1));
+        int64_t *coff = (int64_t *)malloc(sizeof(int64_t) * (size_t)(ncache_cand > 0 ? ncache_cand : 1));
         double *s = (double *)malloc(sizeof(double) * (size_t)(nkeys > 0 ? nkeys : 1));
 
         /* explicit mask, cache part */
@@ -211,7 +241,10 @@ int oracle_attend(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_
                 t = j;
             }
             if (t < cache_begin || t >= cache_end) continue;
-            token[j] = t;
+            if (!cache_row(cl, b, hk, t, &coff[j])) { /* its block is not in the pool */
+                status = ORACLE_BAD_INPUT;
+                continue;
+            }
             visible[j] = 1;
         }
         /* explicit mask, draft part: node i sees itself and its ancestors */
@@ -237,7 +270,7 @@ int oracle_attend(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_
             if (!visible[j]) continue;
             const uint16_t *krow;
             if (j < ncache_cand)
-                krow = k_cache + b * stride_b + hk * stride_h + token[j] * stride_t;
+                krow = k_cache + coff[j];
             else
                 krow = k_draft + (((int64_t)b * N + (j - ncache_cand)) * Hkv + hk) * d;
             double dot = 0.0;
@@ -259,7 +292,7 @@ int oracle_attend(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_
                 if (!visible[j]) continue;
                 const uint16_t *vrow;
                 if (j < ncache_cand)
-                    vrow = v_cache + b * stride_b + hk * stride_h + token[j] * stride_t;
+                    vrow = v_cache + coff[j];
                 else
                     vrow = v_draft + (((int64_t)b * N + (j - ncache_cand)) * Hkv + hk) * d;
                 double p = exp(s[j] - l);
@@ -267,10 +300,39 @@ int oracle_attend(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_
             }
         }
         free(visible);
-        free(token);
+        free(coff);
         free(s);
     }
     return status;
+}
+
+int oracle_attend(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                  int64_t stride_b, int64_t stride_h, int64_t stride_t,
+                  const uint16_t *k_draft, const uint16_t *v_draft, const int32_t *parent,
+                  const int32_t *idx, int budget, int B, int N, int Hq, int Hkv, int d, int L,
+                  const int32_t *ctx_lens, float scale, int64_t cache_begin, int64_t cache_end,
+                  const int64_t *rows, int64_t n_rows, double *out, double *lse)
+{
+    cache_layout cl = {stride_b, stride_h, stride_t, NULL, 0, 0, 0};
+    return attend_core(q, k_cache, v_cache, &cl, k_draft, v_draft, parent, idx, budget, B, N, Hq, Hkv, d,
+                       L, ctx_lens, scale, cache_begin, cache_end, rows, n_rows, out, lse);
+}
+
+/* The same attention over a paged cache: pool strides (elements) for block, KV head and
+   row, the block table [B, table_ld], the block size and the number of pool blocks. */
+int oracle_attend_paged(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
+                        int64_t stride_blk, int64_t stride_h, int64_t stride_row, const int32_t *table,
+                        int64_t table_ld, int block_size, int64_t num_blocks,
+                        const uint16_t *k_draft, const uint16_t *v_draft, const int32_t *parent,
+                        const int32_t *idx, int budget, int B, int N, int Hq, int Hkv, int d, int L,
+                        const int32_t *ctx_lens, float scale, const int64_t *rows, int64_t n_rows,
+                        double *out, double *lse)
+{
+    if (!table || block_size < 1 || num_blocks < 0 || table_ld < (L + block_size - 1) / block_size)
+        return ORACLE_INVALID_ARG;
+    cache_layout cl = {stride_blk, stride_h, stride_row, table, table_ld, block_size, num_blocks};
+    return attend_core(q, k_pool, v_pool, &cl, k_draft, v_draft, parent, idx, budget, B, N, Hq, Hkv, d,
+                       L, ctx_lens, scale, 0, L, rows, n_rows, out, lse);
 }
 
 /* ------------------------------------------------------------------------ */

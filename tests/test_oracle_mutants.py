@@ -38,9 +38,14 @@ MUTANTS = [
      "double wa = exp(la - l), wb = exp(la - l);"),
     ("one extra draft-tier token", "int m = top_m;", "int m = top_m + 1;"),
     ("tier 1 ranks by the target score", "pool[t - rest_lo].score = ds[t];", "pool[t - rest_lo].score = ts[t];"),
-    ("cache V read from K", "vrow = v_cache + b * stride_b", "vrow = k_cache + b * stride_b"),
+    ("cache V read from K", "vrow = v_cache + coff[j];", "vrow = k_cache + coff[j];"),
     ("probability not normalised", "double p = exp(s[j] - l);", "double p = exp(s[j] - mx);"),
     ("sink one short", "for (int t = 0; t < s0; ++t) chosen[t] = 1;", "for (int t = 1; t < s0; ++t) chosen[t] = 1;"),
+    ("paged: row inside the block", "(t % cl->block_size) * cl->st", "((t + 1) % cl->block_size) * cl->st"),
+    ("paged: the next block's entry", "cl->table[b * cl->table_ld + t / cl->block_size]",
+     "cl->table[b * cl->table_ld + t / cl->block_size + 1]"),
+    ("paged: block stride for the head stride", "*off = blk * cl->sb + hk * cl->sh", "*off = blk * cl->sh + hk * cl->sh"),
+    ("paged: an entry one past the pool accepted", "blk >= cl->num_blocks", "blk > cl->num_blocks"),
 ]
 
 PIN_CALLS = [
@@ -57,6 +62,9 @@ PIN_CALLS = [
     pins.test_selection_golden,
     lambda: pins.test_selection_matches_bruteforce(0),
     pins.test_selection_all_equal_scores,
+    lambda: pins.test_paged_equals_contiguous(4),
+    lambda: pins.test_paged_bad_block_entry("pool_size"),
+    pins.test_paged_entries_past_the_context_are_not_read,
 ]
 
 

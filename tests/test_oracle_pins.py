@@ -422,3 +422,75 @@ def test_best_first_is_optimal_and_concave(seed):
         assert abs(sum(t.rho) - _all_prefix_closed_best(marg, n)) < 1e-12
     gains = full.rho  # marginal gain of node n is its rho: non-increasing = concave surrogate
     assert all(g1 >= g2 for g1, g2 in zip(gains, gains[1:]))
+
+
+# ---------------------------------------------------------------------------
+# paged cache (the same cache in fixed-size blocks of a pool, through a block table)
+
+
+def to_pool(kc, vc, bs, gen, extra=3):
+    """Scatter the caches [B, Hkv, L, d] into a pool of blocks of bs rows, in a random block
+    order with `extra` unused blocks of noise and one guard block past the end (never named by
+    a valid entry). Returns (k_pool, v_pool, table [B, nb + 2], num_blocks): table slots past a
+    sequence's blocks hold -7."""
+    B, Hkv, L, d = kc.shape
+    nb = (L + bs - 1) // bs
+    total = B * nb + extra
+    perm = torch.randperm(total, generator=gen)
+    kp = _bf16((total + 1, Hkv, bs, d), gen)
+    vp = _bf16((total + 1, Hkv, bs, d), gen)
+    table = torch.full((B, nb + 2), -7, dtype=torch.int32)
+    for b in range(B):
+        for j in range(nb):
+            blk = int(perm[b * nb + j])
+            table[b, j] = blk
+            t0, t1 = j * bs, min(L, (j + 1) * bs)
+            kp[blk, :, : t1 - t0] = kc[b, :, t0:t1]
+            vp[blk, :, : t1 - t0] = vc[b, :, t0:t1]
+    return kp, vp, table, total
+
+
+@pytest.mark.parametrize("bs", [1, 4, 16])
+def test_paged_equals_contiguous(bs):
+    """Paged = contiguous, bit for bit: dense and sparse, full and ragged contexts."""
+    q, kc, vc, kd, vd, par = tiny_problem(40 + bs, L=37)
+    g = torch.Generator().manual_seed(bs)
+    kp, vp, table, nblk = to_pool(kc, vc, bs, g)
+    cl = torch.tensor([37, 20], dtype=torch.int32)
+    idx = torch.tensor([[0, 3, 4, 9, 17, 30, 36, -1], [1, 2, 5, 8, 13, 19, -1, -1]], dtype=torch.int32)
+    for kw in (dict(), dict(ctx_lens=cl), dict(idx=idx), dict(idx=idx, ctx_lens=cl)):
+        ro, rl, rs = oracle.attend(q, kc, vc, kd, vd, par, scale=0.3, **kw)
+        po, pl, ps = oracle.attend_paged(q, kp, vp, kd, vd, par, table, L=37, scale=0.3, num_blocks=nblk, **kw)
+        assert rs == ps == 0
+        assert np.array_equal(ro, po) and np.array_equal(rl, pl)
+
+
+@pytest.mark.parametrize("bad", [-1, "pool_size"])
+def test_paged_bad_block_entry(bad):
+    """A block entry outside the pool hides its tokens and is reported: the result equals the
+    contiguous sparse attention over the other tokens."""
+    q, kc, vc, kd, vd, par = tiny_problem(50, L=37)
+    bs = 4
+    g = torch.Generator().manual_seed(5)
+    kp, vp, table, nblk = to_pool(kc, vc, bs, g)
+    table[1, 2] = -1 if bad == -1 else nblk
+    po, pl, ps = oracle.attend_paged(q, kp, vp, kd, vd, par, table, L=37, scale=0.3, num_blocks=nblk)
+    assert ps == 5
+    keep = [t for t in range(37) if not 8 <= t < 12]
+    idx = torch.tensor([list(range(37)), keep + [-1] * 4], dtype=torch.int32)
+    ro, rl, rs = oracle.attend(q, kc, vc, kd, vd, par, scale=0.3, idx=idx)
+    assert rs == 0
+    assert np.array_equal(ro, po) and np.array_equal(rl, pl)
+
+
+def test_paged_entries_past_the_context_are_not_read():
+    q, kc, vc, kd, vd, par = tiny_problem(51, L=37)
+    bs = 4
+    g = torch.Generator().manual_seed(6)
+    kp, vp, table, nblk = to_pool(kc, vc, bs, g)
+    cl = torch.tensor([37, 9], dtype=torch.int32)
+    table[1, 3:] = -5  # blocks 3.. of sequence 1 lie past its 9 tokens
+    po, pl, ps = oracle.attend_paged(q, kp, vp, kd, vd, par, table, L=37, scale=0.3, ctx_lens=cl, num_blocks=nblk)
+    ro, rl, rs = oracle.attend(q, kc, vc, kd, vd, par, scale=0.3, ctx_lens=cl)
+    assert ps == rs == 0
+    assert np.array_equal(ro, po) and np.array_equal(rl, pl)
