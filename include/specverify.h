@@ -158,6 +158,46 @@ spec_status_t spec_verify_attn_sparse(const uint16_t *q, const uint16_t *k_cache
                                       void *workspace, size_t ws_bytes, void *stream);
 
 /* ------------------------------------------------------------------------ */
+/* Verification attention with extensions: a paged KV cache and a bf16 output.
+ *
+ * The source pages use neither; they are layouts of serving engines. With
+ * idx == NULL this is spec_verify_attn, with idx != NULL (`budget` entries
+ * per sequence) spec_verify_attn_sparse, and ext == NULL changes nothing.
+ *
+ * ext->block_table != NULL: the cache is paged. The cache of sequence b is
+ * stored in fixed-size blocks of a pool: token t is row t % block_size of
+ * pool block block_table[b * table_ld + t / block_size], and the three
+ * strides describe the pools: element (blk, h, o, c) at blk * kv_stride_b +
+ * h * kv_stride_h + o * kv_stride_t + c (elements, multiples of 8; d
+ * contiguous), 0 <= blk < num_blocks. Only the blocks that hold tokens below
+ * n = ctx_lens[b] are read; a block entry outside [0, num_blocks) hides its
+ * tokens and sets SPEC_ERR_BAD_INPUT in the status word. block_table: int32
+ * [B, table_ld] device, table_ld >= ceil(L / block_size). Requires
+ * kv_stride_t >= 1 and, with idx, kv_stride_b a multiple of kv_stride_t and
+ * num_blocks * (kv_stride_b / kv_stride_t) below 2^31 (else
+ * SPEC_ERR_UNSUPPORTED). The dense tensor-core path takes block sizes that
+ * are multiples of 128 (others run on the warp-level kernel).
+ * ext->out_dtype == SPEC_OUT_BF16: out is bf16 [B, N, Hq, d] (the fp32 result
+ * rounded to nearest even); lse stays fp32.
+ * workspace: >= spec_verify_workspace_size(B, N, Hq, Hkv, d, idx ? budget : L).
+ */
+typedef enum { SPEC_OUT_F32 = 0, SPEC_OUT_BF16 = 1 } spec_out_dtype_t;
+typedef struct {
+    const int32_t *block_table; /* NULL: the contiguous cache of spec_verify_attn */
+    int64_t table_ld;
+    int block_size;
+    int64_t num_blocks;
+    int out_dtype; /* spec_out_dtype_t */
+} spec_verify_ext;
+spec_status_t spec_verify_attn_ex(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                                  int64_t kv_stride_b, int64_t kv_stride_h, int64_t kv_stride_t,
+                                  const uint16_t *k_draft, const uint16_t *v_draft,
+                                  const int32_t *parent, int B, int N, int Hq, int Hkv, int d, int L,
+                                  const int32_t *ctx_lens, float scale, const int32_t *idx,
+                                  int budget, const spec_verify_ext *ext, void *out, float *lse,
+                                  void *workspace, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------ */
 /* Log-sum-exp merge of two normalised attention parts (LongSpec section 2.C):
  *   lse = log(exp(lse_a) + exp(lse_b)),
  *   out = exp(lse_a - lse) * o_a + exp(lse_b - lse) * o_b,

@@ -59,20 +59,30 @@ SplitPlan verify_plan(int B, int N, int Hq, int Hkv, int L_eff, int sms) {
     return make_plan(B, N, Hq, Hkv, L_eff, mma_rows_per_unit(), mma_tile_tokens(), sms * kMmaCtasPerSm);
 }
 
-// Workspace that covers either cache kernel's plan.
+// Workspace that covers either cache kernel's plan, plus (after the partials) room for
+// the resolved index rows of a paged sparse call, [B, L_eff] int32.
 size_t verify_bytes_any(int B, int N, int Hq, int Hkv, int d, int L_eff, int sms) {
     const size_t a = plan_workspace_bytes(verify_plan(B, N, Hq, Hkv, L_eff, sms), d);
     // the slot count does not depend on balancing, so the dense plan sizes both kinds
     const size_t b = plan_workspace_bytes(make_plan_tc(B, N, Hq, Hkv, L_eff, sms, false), d);
-    return std::max(a, b);
+    return std::max(a, b) + align_up((size_t)B * L_eff * sizeof(int32_t), 256);
 }
+
+// Where a paged call's cache lives (all zero for a contiguous cache).
+struct PagedArgs {
+    const int32_t *table = nullptr;
+    int64_t table_ld = 0;
+    int block_size = 0;
+    int64_t num_blocks = 0;
+};
 
 spec_status_t verify_common(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                             int64_t sb, int64_t sh, int64_t st, const uint16_t *k_draft,
                             const uint16_t *v_draft, const int32_t *parent, int B, int N, int Hq,
                             int Hkv, int d, int L, const int32_t *ctx_lens, float scale,
                             const int32_t *idx, int budget, bool sparse, float *out, float *lse,
-                            void *workspace, size_t ws_bytes, void *stream) {
+                            void *workspace, size_t ws_bytes, void *stream, const PagedArgs &pg = PagedArgs(),
+                            bool out_bf16 = false) {
     // host checks, before anything is enqueued
     if (!q || !out || !lse || !workspace) return SPEC_ERR_INVALID_ARG;
     if (B < 1 || N < 1 || N > 4096 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || L < 0) return SPEC_ERR_INVALID_ARG;
@@ -88,6 +98,14 @@ spec_status_t verify_common(const uint16_t *q, const uint16_t *k_cache, const ui
     if (!(scale == scale)) return SPEC_ERR_INVALID_ARG;
     if (d != kHeadDim) return SPEC_ERR_UNSUPPORTED;
     if ((int64_t)B * N * Hq > (int64_t)1 << 31) return SPEC_ERR_INVALID_ARG;
+    if (pg.table) {  // paged cache
+        if (pg.block_size < 1 || pg.num_blocks < 0 || st < 1 || !aligned(pg.table, 4) ||
+            pg.table_ld < ((int64_t)L + pg.block_size - 1) / pg.block_size)
+            return SPEC_ERR_INVALID_ARG;
+        // sparse: index entries become pool rows blk * (sb / st) + o, numbered in 32 bits
+        if (sparse && (sb % st != 0 || pg.num_blocks * (sb / st) + pg.block_size > INT32_MAX))
+            return SPEC_ERR_UNSUPPORTED;
+    }
     DeviceInfo dev;
     if (spec_status_t s = current_device(&dev)) return s;
 
@@ -114,9 +132,26 @@ spec_status_t verify_common(const uint16_t *q, const uint16_t *k_cache, const ui
     a.lse = lse;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     a.status = reinterpret_cast<uint32_t *>(ws);
+    a.table = pg.table;
+    a.table_ld = pg.table_ld;
+    a.block_size = pg.block_size;
+    a.num_blocks = pg.num_blocks;
+    a.idx_resolved = 0;
+    a.out_bf16 = out_bf16 ? 1 : 0;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (const cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s); e != cudaSuccess) return (spec_status_t)cuda_failure(e);
+    if (pg.table && sparse) {
+        // the index set resolved to pool rows (checked there), at the end of the workspace;
+        // the gather kernels then read the pool as one cache of row stride st
+        const size_t rows_bytes = align_up((size_t)B * budget * sizeof(int32_t), 256);
+        int32_t *rows = reinterpret_cast<int32_t *>(ws + (ws_bytes - rows_bytes) / 256 * 256);
+        if (const cudaError_t e = launch_resolve_paged_idx(a, rows, s); e != cudaSuccess) return (spec_status_t)cuda_failure(e);
+        a.idx = rows;
+        a.idx_resolved = 1;
+        a.table = nullptr;
+        a.sb = 0;
+    }
     cudaEvent_t ev0 = g_prof_start && g_prof_stop ? g_prof_start : nullptr;
     cudaEvent_t ev1 = ev0 ? g_prof_stop : nullptr;
     // the tcgen05 kernel when the shape allows it (its TMA maps, its 16-byte row gathers);
@@ -228,6 +263,27 @@ spec_status_t spec_verify_attn_sparse(const uint16_t *q, const uint16_t *k_cache
     return verify_common(q, k_cache, v_cache, kv_stride_b, kv_stride_h, kv_stride_t, k_draft, v_draft,
                          parent, B, N, Hq, Hkv, d, L, ctx_lens, scale, idx, budget, true, out, lse,
                          workspace, ws_bytes, stream);
+}
+
+spec_status_t spec_verify_attn_ex(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                                  int64_t kv_stride_b, int64_t kv_stride_h, int64_t kv_stride_t,
+                                  const uint16_t *k_draft, const uint16_t *v_draft, const int32_t *parent, int B,
+                                  int N, int Hq, int Hkv, int d, int L, const int32_t *ctx_lens, float scale,
+                                  const int32_t *idx, int budget, const spec_verify_ext *ext, void *out, float *lse,
+                                  void *workspace, size_t ws_bytes, void *stream) {
+    PagedArgs pg;
+    bool bf16 = false;
+    if (ext) {
+        if (ext->out_dtype != SPEC_OUT_F32 && ext->out_dtype != SPEC_OUT_BF16) return SPEC_ERR_INVALID_ARG;
+        bf16 = ext->out_dtype == SPEC_OUT_BF16;
+        pg.table = ext->block_table;
+        pg.table_ld = ext->table_ld;
+        pg.block_size = ext->block_size;
+        pg.num_blocks = ext->num_blocks;
+    }
+    return verify_common(q, k_cache, v_cache, kv_stride_b, kv_stride_h, kv_stride_t, k_draft, v_draft, parent, B, N,
+                         Hq, Hkv, d, L, ctx_lens, scale, idx, budget, idx != nullptr, static_cast<float *>(out), lse,
+                         workspace, ws_bytes, stream, pg, bf16);
 }
 
 spec_status_t spec_lse_merge(const float *o_a, const float *lse_a, const float *o_b,

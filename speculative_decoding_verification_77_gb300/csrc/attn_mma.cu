@@ -99,8 +99,6 @@ __global__ void __launch_bounds__(THREADS, 2) cache_attn_mma_kernel(VerifyArgs a
         const int hk = (int)((u / p.row_groups) % a.Hkv);
         const int b = (int)(u / ((int64_t)p.row_groups * a.Hkv));
         const int n = context_len(a, b);
-        const __nv_bfloat16 *kbase = a.k_cache + b * a.sb + hk * a.sh;
-        const __nv_bfloat16 *vbase = a.v_cache + b * a.sb + hk * a.sh;
 
         // Q rows of this unit -> shared memory (zero rows past G*N)
         __syncthreads();
@@ -120,11 +118,14 @@ __global__ void __launch_bounds__(THREADS, 2) cache_attn_mma_kernel(VerifyArgs a
             for (int c = tid; c < BN * 16; c += THREADS) {
                 const int row = c >> 4, ch = c & 15;
                 const int t = cache_token<SPARSE>(a, b, n, tile * BN + row, ch == 0);
-                const bool ok = t >= 0;
+                // the row's offset (paged: through the block table); a row that does not
+                // exist is masked like an unused one
+                const int64_t roff = t >= 0 ? cache_row_offset(a, b, hk, t, ch == 0) : -1;
+                const bool ok = roff >= 0;
                 // a masked row is zero-filled; its (unread) source is a valid address
-                const int64_t off = (int64_t)t * a.st + ch * 8;
-                cp_async16(smem_addr(sK + swz(row, ch)), ok ? (const void *)(kbase + off) : (const void *)a.q, ok);
-                cp_async16(smem_addr(sV + swz(row, ch)), ok ? (const void *)(vbase + off) : (const void *)a.q, ok);
+                const int64_t off = roff + ch * 8;
+                cp_async16(smem_addr(sK + swz(row, ch)), ok ? (const void *)(a.k_cache + off) : (const void *)a.q, ok);
+                cp_async16(smem_addr(sV + swz(row, ch)), ok ? (const void *)(a.v_cache + off) : (const void *)a.q, ok);
                 if (ch == 0) sValid[stage * BN + row] = ok;
             }
             cp_async_commit();

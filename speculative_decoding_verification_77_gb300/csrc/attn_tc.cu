@@ -81,7 +81,7 @@ __device__ __forceinline__ void load_q(const CUtensorMap *tm_q, uint8_t *sQ, uin
     }
 }
 
-template <bool SPARSE>
+template <bool SPARSE, bool PAGED>
 __global__ void __launch_bounds__(THREADS, 1)
 cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
                      const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -137,7 +137,7 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
         __syncwarp();
     } else if (warp == WARP_PRODUCER) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0) produce_dense(bs, sRing, &tm_q, &tm_k, &tm_v, a, p, split_tiles, u_first, g0, g1, qload);
+        if (lane == 0) produce_dense<PAGED>(bs, sRing, &tm_q, &tm_k, &tm_v, a, p, split_tiles, u_first, g0, g1, qload);
         __syncwarp();
     } else if (warp == WARP_MMA) {
         // ------------------------------------------------------------ MMA issuer
@@ -259,9 +259,20 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
 #pragma unroll
                 for (int u4 = 0; u4 < 4; ++u4) raw[u4] = sparse_raw(a, s.b, t0 * T + 32 * u4 + lane);
             }
+            // dense, paged cache: the pool block of this pipe's next tile, loaded one tile ahead
+            auto block_of = [&](int t) -> int {
+                return __ldg(a.table + (int64_t)s.b * a.table_ld + (int64_t)t * T / a.block_size);
+            };
+            int blk_next = (PAGED && warp_rows) ? block_of(seg_tile(s, split_tiles, h, 0)) : 0;
             for (int k = 0; k < s.cnt[h]; ++k) {
                 const int t = seg_tile(s, split_tiles, h, k);
                 uint32_t vmask[4] = {~0u, ~0u, ~0u, ~0u};  // sparse: used index slots of the tile
+                bool bad_block = false;                     // dense, paged: the tile's block is not in the pool
+                if (PAGED && warp_rows) {
+                    bad_block = blk_next < 0 || blk_next >= a.num_blocks;
+                    if (k + 1 < s.cnt[h]) blk_next = block_of(seg_tile(s, split_tiles, h, k + 1));
+                    if (bad_block && t * T < n_ctx && lane == 0) flag_status(a.status, SPEC_ERR_BAD_INPUT);
+                }
                 if (SPARSE && warp_rows) {
 #pragma unroll
                     for (int u4 = 0; u4 < 4; ++u4)
@@ -290,7 +301,8 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
                                     if (!((vmask[c] >> j) & 1u)) r[c][j] = __float_as_uint(-INFINITY);
                         }
                     } else {
-                        const int valid = min(max(n_ctx - t * T, 0), T);  // tokens of this tile inside the context
+                        // tokens of this tile inside the context (none when its block is not in the pool)
+                        const int valid = bad_block ? 0 : min(max(n_ctx - t * T, 0), T);
                         if (valid < T) {  // tail tile (warp-uniform): mask the tokens past the context
 #pragma unroll
                             for (int c = 0; c < 4; ++c)
@@ -429,6 +441,8 @@ bool tc_supported(const VerifyArgs &a) {
     if (!(a.G >= 1 && a.G <= 128 && (128 % a.G) == 0 && a.scale > 0.f)) return false;
     if (a.idx)  // gathered rows are copied 16 bytes at a time: every row start 16-byte aligned
         return a.budget >= 1 && a.sb % 8 == 0 && a.sh % 8 == 0 && a.st % 8 == 0;
+    // paged: a 128-token tile must lie in one block, and the block coordinate is 32-bit
+    if (a.table && (a.block_size % T != 0 || a.num_blocks < 1 || a.num_blocks > INT32_MAX)) return false;
     return a.L >= 1;
 }
 
@@ -447,7 +461,9 @@ cudaError_t launch_cache_attn_tc(const VerifyArgs &a, const SplitPlan &p, cudaSt
         mk = mq;
         mv = mq;
     } else {
-        const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)a.L, (cuuint64_t)a.Hkv, (cuuint64_t)a.B};
+        // contiguous cache [B, Hkv, L, d] or (paged) the pool [blocks, Hkv, block_size, d]
+        const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)(a.table ? a.block_size : a.L), (cuuint64_t)a.Hkv,
+                                    (cuuint64_t)(a.table ? a.num_blocks : a.B)};
         const cuuint64_t strides[3] = {(cuuint64_t)a.st * 2, (cuuint64_t)a.sh * 2, (cuuint64_t)a.sb * 2};
         const cuuint32_t box[4] = {64, (cuuint32_t)T, 1, 1};
         if (!encode_map(&mk, a.k_cache, 4, dims, strides, box)) return cudaSuccess;
@@ -456,11 +472,13 @@ cudaError_t launch_cache_attn_tc(const VerifyArgs &a, const SplitPlan &p, cudaSt
     TcParams tp;
     tp.M = a.G * a.N;
     tp.split_tiles = tp.M <= 128 ? 1 : 0;
-    auto kern = sparse ? cache_attn_tc_kernel<true> : cache_attn_tc_kernel<false>;
+    auto kern = sparse ? cache_attn_tc_kernel<true, false>
+                       : (a.table ? cache_attn_tc_kernel<false, true> : cache_attn_tc_kernel<false, false>);
     static PerDeviceOnce attr_once;
     cudaError_t e = once_per_device(attr_once, [] {
-        const cudaError_t r = kernel_attributes(cache_attn_tc_kernel<false>, SMEM_BYTES);
-        return r != cudaSuccess ? r : kernel_attributes(cache_attn_tc_kernel<true>, SMEM_BYTES);
+        cudaError_t r = kernel_attributes(cache_attn_tc_kernel<false, false>, SMEM_BYTES);
+        if (r == cudaSuccess) r = kernel_attributes(cache_attn_tc_kernel<false, true>, SMEM_BYTES);
+        return r != cudaSuccess ? r : kernel_attributes(cache_attn_tc_kernel<true, false>, SMEM_BYTES);
     });
     if (e != cudaSuccess) return e;
     if (ev0) cudaEventRecord(ev0, s);

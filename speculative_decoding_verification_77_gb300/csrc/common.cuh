@@ -212,6 +212,14 @@ struct VerifyArgs {
     uint32_t *status;
     float *o_part;    // [slots][BM][d]
     float *lse_part;  // [slots][BM]
+    // paged cache (table != nullptr): token t of sequence b is row t % block_size of pool
+    // block table[b * table_ld + t / block_size]; sb is then the pool's block stride
+    const int32_t *table;
+    int64_t table_ld;
+    int block_size;
+    int64_t num_blocks;
+    int idx_resolved;  // sparse: idx holds validated pool rows (entry >= 0: used), see paged.cu
+    int out_bf16;      // out is bf16 [B, N, Hq, d] (rounded to nearest even) instead of fp32
 };
 
 // Context length of sequence b, clamped to [0, L]; out-of-range values flag bad input.
@@ -232,6 +240,7 @@ __device__ __forceinline__ int sparse_token(const VerifyArgs &a, int b, int n, i
     if (j >= a.budget) return -1;
     const int32_t *ib = a.idx + (int64_t)b * a.budget;
     const int t = __ldg(ib + j);
+    if (a.idx_resolved) return t >= 0 ? t : -1;  // checked (and reported) when it was resolved
     const bool ok = t >= 0 && t < n && (j == 0 || t > __ldg(ib + j - 1));
     if (!ok && t != -1 && report) flag_status(a.status, SPEC_ERR_BAD_INPUT);
     return ok ? t : -1;
@@ -254,9 +263,23 @@ __device__ __forceinline__ IdxPair sparse_raw(const VerifyArgs &a, int b, int j)
 // ... then the token (or -1) once they have arrived.
 __device__ __forceinline__ int sparse_resolve(const VerifyArgs &a, IdxPair r, int j, int n, bool report) {
     if (j >= a.budget) return -1;
+    if (a.idx_resolved) return r.cur >= 0 ? r.cur : -1;  // checked (and reported) when it was resolved
     const bool ok = r.cur >= 0 && r.cur < n && (j == 0 || r.cur > r.prev);
     if (!ok && r.cur != -1 && report) flag_status(a.status, SPEC_ERR_BAD_INPUT);
     return ok ? r.cur : -1;
+}
+
+// Element offset of the cache row of token t (sequence b, KV head hk), or -1 when the
+// row does not exist (paged: its block entry is outside the pool, recorded as bad input
+// when `report`).
+__device__ __forceinline__ int64_t cache_row_offset(const VerifyArgs &a, int b, int hk, int t, bool report) {
+    if (!a.table) return (int64_t)b * a.sb + (int64_t)hk * a.sh + (int64_t)t * a.st;
+    const int64_t blk = __ldg(a.table + (int64_t)b * a.table_ld + t / a.block_size);
+    if (blk < 0 || blk >= a.num_blocks) {
+        if (report) flag_status(a.status, SPEC_ERR_BAD_INPUT);
+        return -1;
+    }
+    return blk * a.sb + (int64_t)hk * a.sh + (int64_t)(t % a.block_size) * a.st;
 }
 
 // Tiling of the mma.sync cache kernel (query rows per unit, tokens per tile).
@@ -308,6 +331,9 @@ cudaError_t launch_lse_merge2(const float *o_a, const float *lse_a, const float 
 bool launch_select_cluster_reg(const float *ds, const float *ts, int64_t ld, int B, int L, const int32_t *ctx_lens,
                                int sink, int window, int top_m, int budget, int32_t *idx, int32_t *count,
                                uint32_t *status, cudaStream_t s, cudaError_t *err);
+// Paged sparse calls: idx [B, budget] -> the pool rows of its used entries (-1 otherwise),
+// see paged.cu.
+cudaError_t launch_resolve_paged_idx(const VerifyArgs &a, int32_t *rows_out, cudaStream_t s);
 cudaError_t launch_select_topk(const float *ds, const float *ts, int64_t ld, int B, int L,
                                const int32_t *ctx_lens, int sink, int window, int top_m,
                                int budget, int32_t *idx, int32_t *count, uint32_t *status,

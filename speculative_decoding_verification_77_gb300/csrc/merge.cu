@@ -257,7 +257,16 @@ __global__ void __launch_bounds__(256) merge_tree_kernel(VerifyArgs a, SplitPlan
             o = make_float4(st.acc[j].x * inv, st.acc[j].y * inv, st.acc[j].z * inv, st.acc[j].w * inv);
             l = st.m[j] + __logf(st.s[j]);
         }
-        *reinterpret_cast<float4 *>(a.out + (out_row0 + j) * kHeadDim + 4 * lane) = o;
+        const int64_t e0 = (out_row0 + j) * kHeadDim + 4 * lane;  // first of this lane's 4 elements
+        if (a.out_bf16) {
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y), hi = __floats2bfloat162_rn(o.z, o.w);
+            uint2 w;
+            w.x = *reinterpret_cast<const uint32_t *>(&lo);
+            w.y = *reinterpret_cast<const uint32_t *>(&hi);
+            *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(a.out) + e0) = w;
+        } else {
+            *reinterpret_cast<float4 *>(a.out + e0) = o;
+        }
         if (lane == 0) a.lse[out_row0 + j] = l;
     }
 }

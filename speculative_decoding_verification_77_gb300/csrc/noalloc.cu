@@ -114,6 +114,12 @@ extern "C" spec_status_t spec_verify_attn_noalloc(
     a.out = out;
     a.lse = lse;
     a.status = reinterpret_cast<uint32_t *>(ws);
+    a.table = nullptr;
+    a.table_ld = 0;
+    a.block_size = 0;
+    a.num_blocks = 0;
+    a.idx_resolved = 0;
+    a.out_bf16 = 0;
     a.o_part = reinterpret_cast<float *>(ws + kHeaderBytes);
     a.lse_part = reinterpret_cast<float *>(ws + kHeaderBytes +
                                            align_up((size_t)plan.slots * plan.BM * d * sizeof(float), 256));

@@ -175,7 +175,7 @@ __device__ __forceinline__ void produce_sparse(Bars &bs, uint8_t *sRing, const C
 
 // TMA producer (one thread): the K and V tiles of the CTA's range, and each
 // unit's Q through qload(seg, buffer, bar).
-template <class QLoad>
+template <bool PAGED, class QLoad>
 __device__ __forceinline__ void produce_dense(Bars &bs, uint8_t *sRing, const CUtensorMap *tm_q, const CUtensorMap *tm_k,
                                               const CUtensorMap *tm_v, const VerifyArgs &a, const SplitPlan &p,
                                               int split_tiles, int64_t u_first, int64_t g0, int64_t g1, QLoad qload) {
@@ -195,8 +195,20 @@ __device__ __forceinline__ void produce_dense(Bars &bs, uint8_t *sRing, const CU
         q_buffer(split_tiles, q_loads, qb, quse);
         if (quse > 0 && !(ok = wait_bar(bs, &bs.q_empty[qb], (quse - 1) & 1, a.status))) break;
         qload(s, qb, &bs.q_full[qb]);
+        // paged cache: the pool block of each tile (a tile lies in one block), loaded four
+        // tiles ahead of its use
+        auto block_of = [&](int t) -> int {
+            if (!PAGED || t >= s.te) return 0;
+            return __ldg(a.table + (int64_t)s.b * a.table_ld + (int64_t)t * T / a.block_size);
+        };
+        int blk0 = block_of(s.tb), blk1 = block_of(s.tb + 1), blk2 = block_of(s.tb + 2), blk3 = block_of(s.tb + 3);
         // K and V tiles in order: tile tb: K, V; tile tb+1: K, V; ...
         for (int t = s.tb; t < s.te; ++t) {
+            const int blk = blk0;
+            blk0 = blk1;
+            blk1 = blk2;
+            blk2 = blk3;
+            blk3 = block_of(t + 4);
             for (int kv = 0; kv < 2; ++kv, ++item) {
                 const int slot = (int)(item % RING);
                 const int64_t use = item / RING;
@@ -205,8 +217,15 @@ __device__ __forceinline__ void produce_dense(Bars &bs, uint8_t *sRing, const CU
                 uint8_t *dst = sRing + slot * SLOT_BYTES;
                 mbar_arrive_expect_tx(&bs.kv_full[slot], SLOT_BYTES);
                 const CUtensorMap *m = kv == 0 ? tm_k : tm_v;
-                tma_load_4d(dst, m, &bs.kv_full[slot], 0, t * T, s.hk, s.b);
-                tma_load_4d(dst + HALF_BYTES, m, &bs.kv_full[slot], 64, t * T, s.hk, s.b);
+                if (PAGED) {  // pool map [blocks, Hkv, block_size, d]: a block entry outside the pool
+                                // reads the zero fill (the softmax masks that tile)
+                    const int o = (int)((int64_t)t * T % a.block_size);
+                    tma_load_4d(dst, m, &bs.kv_full[slot], 0, o, s.hk, blk);
+                    tma_load_4d(dst + HALF_BYTES, m, &bs.kv_full[slot], 64, o, s.hk, blk);
+                } else {
+                    tma_load_4d(dst, m, &bs.kv_full[slot], 0, t * T, s.hk, s.b);
+                    tma_load_4d(dst + HALF_BYTES, m, &bs.kv_full[slot], 64, t * T, s.hk, s.b);
+                }
             }
             if (!ok) break;
         }

@@ -10,6 +10,7 @@ Names mirror the C ABI (include/specverify.h):
   select_topk            -> spec_select_topk
   verify_attn            -> spec_verify_attn
   verify_attn_sparse     -> spec_verify_attn_sparse
+  verify_attn_ex         -> spec_verify_attn_ex (paged cache, bf16 output)
   lse_merge              -> spec_lse_merge
   accept_commit          -> spec_accept_commit
   budget_plan            -> spec_budget_plan (host)
@@ -44,6 +45,7 @@ SIGNATURES = {
     "spec_verify_attn_sparse": (I, [P, P, P, I64, I64, I64, P, P, P, I, I, I, I, I, I, P, F, P, I,
                                     P, P, P, SZ, P]),
     "spec_lse_merge": (I, [P, P, P, P, P, P, I64, I, P]),
+    "spec_verify_attn_ex": (I, [P, P, P, I64, I64, I64, P, P, P, I, I, I, I, I, I, P, F, P, I, P, P, P, P, SZ, P]),
     "spec_verify_attn_noalloc": (I, [P, P, P, I64, I64, I64, P, P, P, I, I, I, I, I, I, P, F, P, P, P, P]),
     "spec_read_device_status": (I, [P, P]),
     "spec_accept_commit": (I, [P, P, P, I, I, P, P, P, P, P, I64, I64, I64, P, P, I, I, I, P, P, P]),
@@ -207,6 +209,77 @@ def verify_attn_sparse(q, k_cache, v_cache, k_draft, v_draft, parent, idx, *, sc
                        ctx_lens=None, out=None, lse=None, ws=None):
     """Sparse verification attention over the cache rows idx[b] (int32 [B, budget])."""
     return _verify(q, k_cache, v_cache, k_draft, v_draft, parent, scale, ctx_lens, idx, out, lse, ws)
+
+
+class _VerifyExt(ctypes.Structure):
+    _fields_ = [("block_table", ctypes.c_void_p), ("table_ld", ctypes.c_int64), ("block_size", ctypes.c_int),
+                ("num_blocks", ctypes.c_int64), ("out_dtype", ctypes.c_int)]
+
+
+def verify_attn_ex(q, k_cache, v_cache, k_draft=None, v_draft=None, parent=None, *, L: int | None = None, idx=None,
+                   block_table=None, out_dtype=torch.float32, scale=None, ctx_lens=None, out=None, lse=None, ws=None):
+    """Verification attention with the extensions of spec_verify_attn_ex: a paged cache and/or a
+    bf16 output (dense, or sparse with idx [B, budget]).
+
+    Contiguous: k_cache/v_cache [B, Hkv, L, d]. Paged (block_table int32 [B, max_blocks]):
+    k_cache/v_cache are the pools, [num_blocks, Hkv, block_size, d] bf16 views (any strides, d
+    contiguous; a token-major pool [num_blocks, block_size, Hkv, d] is passed permuted); token t of
+    sequence b is row t % block_size of block block_table[b, t // block_size], and L (the longest
+    context) must be given. out_dtype torch.float32 or torch.bfloat16.
+    Returns (out [B,N,Hq,d] of out_dtype, lse fp32 [B,N,Hq]).
+    """
+    lib = load_library()
+    for t, nm in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (k_draft, "k_draft"), (v_draft, "v_draft")):
+        _need(t, torch.bfloat16, nm, 4)
+    _need(block_table, torch.int32, "block_table", 2)
+    _need(parent, torch.int32, "parent", 2)
+    _need(ctx_lens, torch.int32, "ctx_lens", 1)
+    _need(idx, torch.int32, "idx", 2)
+    if out_dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("out_dtype must be torch.float32 or torch.bfloat16")
+    B, N, Hq, d = q.shape
+    if block_table is None:
+        _, Hkv, Lc, _ = k_cache.shape
+        L = Lc if L is None else L
+        nblk = bs = 0
+    else:
+        nblk, Hkv, bs, _ = k_cache.shape
+        if L is None:
+            raise ValueError("a paged call needs L, the longest context")
+        if block_table.stride(1) != 1 or block_table.shape[0] != B:
+            raise ValueError("block_table must be [B, max_blocks] with unit column stride")
+    if not q.is_contiguous():
+        raise ValueError("q must be contiguous [B, N, Hq, d]")
+    if k_cache.stride() != v_cache.stride() or k_cache.shape != v_cache.shape or k_cache.stride(3) != 1:
+        raise ValueError("k_cache and v_cache must share shape and strides, with d contiguous")
+    if idx is not None and (not idx.is_contiguous() or idx.shape[0] != B):
+        raise ValueError("idx must be contiguous int32 [B, budget]")
+    if scale is None:
+        scale = d ** -0.5
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, N, Hq, d), dtype=out_dtype, device=dev)
+    _need(out, out_dtype, "out", 4)
+    if lse is None:
+        lse = torch.empty((B, N, Hq), dtype=torch.float32, device=dev)
+    L_eff = idx.shape[1] if idx is not None else L
+    nbytes = lib.spec_verify_workspace_size(B, N, Hq, Hkv, d, L_eff)
+    if ws is None:
+        ws = workspace(nbytes, dev, "verify")
+    ext = _VerifyExt(None if block_table is None else block_table.data_ptr(),
+                     0 if block_table is None else block_table.stride(0), bs, nblk,
+                     1 if out_dtype == torch.bfloat16 else 0)
+    code = lib.spec_verify_attn_ex(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.stride(0), k_cache.stride(1), k_cache.stride(2), _ptr(k_draft),
+        _ptr(v_draft), _ptr(parent), B, N, Hq, Hkv, d, L, _ptr(ctx_lens), ctypes.c_float(scale), _ptr(idx),
+        0 if idx is None else idx.shape[1], ctypes.byref(ext), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(q))
+    _check("spec_verify_attn_ex", code)
+    return out, lse
+
+
+def verify_attn_paged(q, k_pool, v_pool, block_table, k_draft=None, v_draft=None, parent=None, *, L: int, **kw):
+    """verify_attn_ex over a paged cache (see there)."""
+    return verify_attn_ex(q, k_pool, v_pool, k_draft, v_draft, parent, L=L, block_table=block_table, **kw)
 
 
 def lse_merge(o_a, lse_a, o_b, lse_b, out=None, lse_out=None):

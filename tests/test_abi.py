@@ -132,6 +132,28 @@ def test_noalloc_rejects_bad_arguments_on_the_host(lib, over, code):
     assert lib.spec_verify_attn_noalloc(*a.values()) == code
 
 
+@pytest.mark.parametrize("over,code", [
+    (dict(bs=0), 1), (dict(ld=1, L=300), 1), (dict(st=0), 1), (dict(d=64), 2), (dict(sb=1001), 1),
+    (dict(dtype=7), 1),
+    # sparse: the block stride must be a multiple of the row stride (pool rows are numbered)
+    (dict(idx=16, budget=4, sb=1032, st=16), 2),
+])
+def test_paged_rejects_bad_arguments_on_the_host(lib, over, code):
+    # fake, never-dereferenced addresses: every one of these checks returns before any CUDA call
+    from speculative_decoding_verification_77_gb300 import ops
+
+    e = dict(table=16, ld=4, bs=128, nblk=8, dtype=0)
+    for k in e:
+        if k in over:
+            e[k] = over.pop(k)
+    ext = ops._VerifyExt(e["table"], e["ld"], e["bs"], e["nblk"], e["dtype"])
+    a = dict(q=16, kp=16, vp=16, sb=128 * 128, sh=128 * 128, st=128, kd=None, vd=None, par=None, B=1, N=1, Hq=1,
+             Hkv=1, d=128, L=300, ctx=None, scale=ctypes.c_float(0.1), idx=None, budget=0, ext=ctypes.byref(ext),
+             out=16, lse=16, ws=256, ws_bytes=1 << 30, stream=None)
+    a.update(over)
+    assert lib.spec_verify_attn_ex(*a.values()) == code
+
+
 def test_merge_rejects_bad_arguments_on_the_host(lib):
     assert lib.spec_lse_merge(None, 4, 4, 4, 4, 4, 10, 128, None) == 1
     assert lib.spec_lse_merge(4, 4, 4, 4, 4, 4, -1, 128, None) == 1

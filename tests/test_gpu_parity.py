@@ -582,3 +582,102 @@ def test_importance_scores_match_oracle(ops, case):
         assert np.all(got[b, ctx[b]:] == 0.0)
     assert np.allclose(got, want, rtol=1e-4, atol=1e-6), np.abs(got - want).max()
     assert want.max() > 0
+
+
+# ---------------------------------------------------------------- paged KV cache
+
+def paged_case(seed, B, N, Hq, Hkv, L, bs, token_major=False, depth=4):
+    """A contiguous problem and the same cache scattered into a pool of bs-row blocks in a random
+    order (noise blocks in between): (x, k_pool view, v_pool view [nblk, Hkv, bs, d] on the device,
+    block table, number of pool blocks)."""
+    from tests.test_oracle_pins import to_pool
+
+    x = small(seed, B=B, N=N, Hq=Hq, Hkv=Hkv, L=L, depth=depth)
+    g = torch.Generator().manual_seed(seed)
+    kp, vp, table, nblk = to_pool(x["k_cache"], x["v_cache"], bs, g)
+    kp, vp = kp[:nblk], vp[:nblk]
+    if token_major:  # pool memory [nblk, bs, Hkv, d], seen as [nblk, Hkv, bs, d]
+        gk = kp.permute(0, 2, 1, 3).contiguous().to(dev()).permute(0, 2, 1, 3)
+        gv = vp.permute(0, 2, 1, 3).contiguous().to(dev()).permute(0, 2, 1, 3)
+    else:
+        gk, gv = kp.to(dev()), vp.to(dev())
+    return x, kp, vp, gk, gv, table, nblk
+
+
+@pytest.mark.parametrize("case", ["dense_bs128", "dense_bs256_token_major", "dense_bs16", "dense_g3",
+                                  "sparse_bs16", "sparse_bs128_token_major", "bad_block_dense", "bad_block_sparse"])
+def test_paged_cache_matches_oracle(ops, case):
+    """Paged cache on both cache kernels (tensor-core tiles need blocks of a multiple of 128 rows)
+    against the paged oracle, which is pinned to the contiguous one bit for bit."""
+    Hq, Hkv = (12, 4) if case == "dense_g3" else (8, 2)
+    bs = int(case.split("_bs")[1].split("_")[0]) if "_bs" in case else 128
+    B, N, L = 2, 6, 1000
+    x, kp, vp, gk, gv, table, nblk = paged_case(100 + bs, B, N, Hq, Hkv, L, bs, "token_major" in case)
+    cl = torch.tensor([L, 777], dtype=torch.int32)
+    idx = None
+    if "sparse" in case:
+        ds, ts = W.random_scores(B, L, seed=bs)
+        idx, _, _ = oracle.select(ds, ts, ctx_lens=cl, sink=4, window=32, top_m=100, budget=300)
+        idx = torch.from_numpy(idx)
+    if case.startswith("bad_block"):
+        table[1, 3] = nblk  # a block inside sequence 1's context that the pool does not have
+    g = to_dev(x)
+    out, lse = ops.verify_attn_paged(g["q"], gk, gv, table.to(dev()), g["k_draft"], g["v_draft"], g["parent"], L=L,
+                                     idx=None if idx is None else idx.to(dev()), scale=x["scale"],
+                                     ctx_lens=cl.to(dev()))
+    ro, rl, st = oracle.attend_paged(x["q"], kp, vp, x["k_draft"], x["v_draft"], x["parent"], table, L=L,
+                                     scale=x["scale"], ctx_lens=cl, idx=idx)
+    assert st == (5 if case.startswith("bad_block") else 0)
+    ws = ops.workspace(0, dev(), "verify")
+    assert ops.read_device_status(ws) == st
+    assert_attn_close(out, lse, ro, rl)
+
+
+def test_paged_headline_shape_sampled(ops):
+    """The headline layer's shape (B=4, L=32k, 32/8 heads, N=64 tree) on a pool of 256-row blocks."""
+    w = W.workload(2)
+    x = W.make_inputs(w)
+    from tests.test_oracle_pins import to_pool
+
+    g0 = torch.Generator().manual_seed(2)
+    kp, vp, table, nblk = to_pool(x["k_cache"], x["v_cache"], 256, g0)
+    kp, vp = kp[:nblk], vp[:nblk]
+    g = to_dev(x)
+    out, lse = ops.verify_attn_paged(g["q"], kp.to(dev()), vp.to(dev()), table.to(dev()), g["k_draft"],
+                                     g["v_draft"], g["parent"], L=w.L, scale=x["scale"])
+    rows = unit_rows(w, 8, seed=5)
+    ro, rl, st = oracle.attend_paged(x["q"], kp, vp, x["k_draft"], x["v_draft"], x["parent"], table, L=w.L,
+                                     scale=x["scale"], rows=rows)
+    assert st == 0
+    assert_attn_close(out, lse, ro, rl, rows)
+
+
+@pytest.mark.parametrize("case", ["dense_tc", "dense_g3", "sparse", "paged"])
+def test_bf16_output_is_the_rounded_fp32_output(ops, case):
+    """out_dtype bf16: the fp32 result of the same call rounded to nearest even, bit for bit, and
+    within the oracle tolerance plus one bf16 rounding of |o|."""
+    Hq, Hkv = (12, 4) if case == "dense_g3" else (8, 2)
+    x = small(200, B=2, N=5, Hq=Hq, Hkv=Hkv, L=900)
+    g = to_dev(x)
+    kc, vc, kw, okw = g["k_cache"], g["v_cache"], {}, {}
+    if case == "sparse":
+        ds, ts = W.random_scores(2, 900, seed=3)
+        idx, _, _ = oracle.select(ds, ts, sink=4, window=16, top_m=64, budget=256)
+        kw["idx"] = torch.from_numpy(idx).to(dev())
+        okw["idx"] = torch.from_numpy(idx)
+    if case == "paged":
+        from tests.test_oracle_pins import to_pool
+
+        kp, vp, table, nblk = to_pool(x["k_cache"], x["v_cache"], 128, torch.Generator().manual_seed(9))
+        kc, vc = kp[:nblk].to(dev()), vp[:nblk].to(dev())
+        kw.update(block_table=table.to(dev()), L=900)
+    args = (g["q"], kc, vc, g["k_draft"], g["v_draft"], g["parent"])
+    o32, l32 = ops.verify_attn_ex(*args, scale=x["scale"], **kw)
+    o16, l16 = ops.verify_attn_ex(*args, scale=x["scale"], out_dtype=torch.bfloat16, **kw)
+    torch.cuda.synchronize()
+    assert o16.dtype == torch.bfloat16
+    assert torch.equal(o16, o32.to(torch.bfloat16)) and torch.equal(l16, l32)
+    ro, rl, _ = oracle.attend(x["q"], x["k_cache"], x["v_cache"], x["k_draft"], x["v_draft"], x["parent"],
+                              scale=x["scale"], **okw)
+    o = o16.float().cpu().numpy().reshape(ro.shape)
+    assert np.abs(o - ro).max() <= ATOL_O + np.abs(ro).max() * 2.0 ** -8
