@@ -372,6 +372,39 @@ def time_extra(case, stream, args, peaks, peak_src, clocks_windows):
     return e
 
 
+def time_importance(dev, stream, args, peaks, peak_src, windows):
+    """The importance-score producer at the headline layer (B=4, L=32k, N=64): two listed heads
+    of different KV heads, lse from the verify call. Algorithmic bytes: the K rows of the two
+    heads' KV heads, 2 x B x L x 256 B."""
+    from speculative_decoding_verification_77_gb300 import ops
+
+    w = W.workload(2)
+    case = Case(w, dev)
+    _, lse = case.attend(case.g)
+    heads = torch.tensor([3, 17], dtype=torch.int32, device=dev)
+    score = torch.empty((w.B, w.L), dtype=torch.float32, device=dev)
+
+    def run(t):
+        ops.importance_scores(t["q"], t["k_cache"], lse, heads, scale=case.scale, out=score)
+
+    for _ in range(3):
+        run(case.g)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    v = time_loop(case, run, stream, args.steps, args.extra_seconds / 2)
+    t1 = time.time()
+    ms = sum(v) / len(v)
+    kbytes = 2 * w.B * w.L * w.d * 2
+    gbs = kbytes / (ms * 1e-3) / 1e9
+    e = {"workload": w.name + " importance scores, heads [3, 17]", "us_per_call": round(ms * 1e3, 2),
+         "k_bytes": kbytes, "achieved_gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
+         "kernel": "importance_tc (tcgen05: S^T = K Q^T per 128-token tile, TMEM lane per token)",
+         "peaks": f"{peak_src}: hbm {peaks['hbm_gbs']} GB/s", "calls_timed": len(v)}
+    windows.append((e, t0, t1))
+    case.release()
+    return e
+
+
 def bastion_calibration(sweep, marginals, peaks, args):
     """BASTION's budget controller calibrated on the measured tree-size sweep: T_verify(N) =
     a T_roof(N) + c fitted to the sweep's step times, then the best-first growth and the
@@ -469,6 +502,8 @@ def run_native(args, ws_, rank, local):
                 extras[wx.name] = e
                 cx.release()
                 del cx
+        if 2 in wanted:
+            extras["importance-scores-llama3-8b-layer"] = time_importance(dev, stream, args, peaks, peak_src, windows)
         if sweep and marginals is not None:
             head_e = None
             if w.tree == "best_first" and w.name.startswith("tree-sweep"):

@@ -339,6 +339,12 @@ cudaError_t launch_select_topk(const float *ds, const float *ts, int64_t ld, int
                                int budget, int32_t *idx, int32_t *count, uint32_t *status,
                                cudaStream_t s);
 
+// Importance scores on the tensor core; false (nothing launched) for shapes it does not take.
+bool launch_importance_tc(const __nv_bfloat16 *q, const __nv_bfloat16 *k_cache, int64_t sb, int64_t sh, int64_t st,
+                          const float *lse, const int32_t *heads, int nh, int B, int N, int Hq, int Hkv, int L,
+                          const int32_t *ctx_lens, float scale, float *score, int64_t ld, int32_t *status,
+                          int sms, cudaStream_t s, cudaError_t *err);
+
 // Kernel-launch counter (per host thread), see spec_kernel_launches().
 void count_launches(int n);
 

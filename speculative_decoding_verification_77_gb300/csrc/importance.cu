@@ -9,12 +9,12 @@
 // exp(scale q[b,i,h] . k[b, h / G, t] - lse[b,i,h]), with lse as the verify call
 // returns it. Rows with lse = -inf (nothing attended) add nothing.
 //
-// A second pass over the K rows of the listed heads, after the verify call.
-// One thread per token: the token's K row sits in registers, each head's
-// queries and lse are staged in shared memory and read as broadcasts, and the
-// dot products run on the FMA pipe in fp32. This first form is bound by those
-// FMAs (N x d per token and head); the contraction is dense and its tensor-core
-// form is the next step.
+// A second pass over the K rows of the listed heads, after the verify call. The
+// tensor-core form (importance_tc.cu) takes the call when the listed heads'
+// queries fit its staging (heads x queries padded to 16 <= 256 rows); this file
+// keeps the portable form for the other shapes: one thread per token, the token's
+// K row in registers, each head's queries and lse staged in shared memory and
+// read as broadcasts, fp32 dot products on the FMA pipe.
 #include "common.cuh"
 
 namespace specverify {
@@ -115,6 +115,16 @@ extern "C" spec_status_t spec_importance_scores(const uint16_t *q, const uint16_
             return (spec_status_t)cuda_failure(e);
     }
     if (L == 0) return SPEC_OK;
+    if (nh > 0) {  // the tensor-core form where the shape allows it
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return (spec_status_t)cuda_failure(cudaGetLastError());
+        cudaError_t e;
+        if (launch_importance_tc(reinterpret_cast<const __nv_bfloat16 *>(q), reinterpret_cast<const __nv_bfloat16 *>(k_cache),
+                                 kv_stride_b, kv_stride_h, kv_stride_t, lse, heads, nh, B, N, Hq, Hkv, L, ctx_lens, scale,
+                                 score, ld, status, sms, s, &e))
+            return e == cudaSuccess ? SPEC_OK : (spec_status_t)cuda_failure(e);
+    }
     const size_t smem = (size_t)N * 256 + (size_t)N * sizeof(float);
     static PerDeviceOnce attr_once;
     const cudaError_t attr = once_per_device(

@@ -553,14 +553,22 @@ def test_accept_commit_matches_oracle(ops, case):
 
 # ---------------------------------------------------------------- importance scores
 
-@pytest.mark.parametrize("case", ["ragged", "repeated_heads_g8", "bad_head"])
+@pytest.mark.parametrize("case", ["ragged", "repeated_heads_g8", "bad_head", "n24_tail", "fma_form_n200",
+                                  "draft_lookahead"])
 def test_importance_scores_match_oracle(ops, case):
-    """Target-historical scores on the listed heads. Both sides read the same lse: the attention
-    oracle's, rounded to fp32 (the dtype the library takes)."""
+    """Target-historical scores on the listed heads (tensor-core form; fma_form_n200 stages more
+    than 256 query rows and takes the portable form). Both sides read the same lse: the attention
+    oracle's, rounded to fp32 (the dtype the library takes). draft_lookahead feeds the call a
+    drafter's own queries, keys and lse (one KV head, four query heads): the same computation
+    gives the draft-lookahead signal."""
     shapes = {"ragged": dict(B=2, N=8, Hq=8, Hkv=2, L=3000),
               "repeated_heads_g8": dict(B=1, N=16, Hq=16, Hkv=2, L=1500),
-              "bad_head": dict(B=2, N=4, Hq=8, Hkv=2, L=700)}[case]
-    heads = {"ragged": [1, 6], "repeated_heads_g8": [0, 9, 9, 15], "bad_head": [2, 99]}[case]
+              "bad_head": dict(B=2, N=4, Hq=8, Hkv=2, L=700),
+              "n24_tail": dict(B=2, N=24, Hq=8, Hkv=4, L=1111),
+              "fma_form_n200": dict(B=1, N=200, Hq=8, Hkv=2, L=900),
+              "draft_lookahead": dict(B=2, N=8, Hq=4, Hkv=1, L=2500)}[case]
+    heads = {"ragged": [1, 6], "repeated_heads_g8": [0, 9, 9, 15], "bad_head": [2, 99], "n24_tail": [7, 0, 3],
+             "fma_form_n200": [1, 5], "draft_lookahead": [0, 1, 2, 3]}[case]
     x = small(91, depth=3, **shapes)
     B, N, Hq, L = shapes["B"], shapes["N"], shapes["Hq"], shapes["L"]
     ctx = np.array([L, 1234][:B] if case == "ragged" else [L] * B, np.int32)
@@ -681,3 +689,27 @@ def test_bf16_output_is_the_rounded_fp32_output(ops, case):
                               scale=x["scale"], **okw)
     o = o16.float().cpu().numpy().reshape(ro.shape)
     assert np.abs(o - ro).max() <= ATOL_O + np.abs(ro).max() * 2.0 ** -8
+
+
+def test_importance_scores_headline_shape(ops):
+    """The headline layer (B=4, L=32k, N=64 tree) scored on two heads of different KV heads,
+    against the oracle on a sample of tokens of every sequence (all draft queries of each)."""
+    w = W.workload(2)
+    x = W.make_inputs(w)
+    g = to_dev(x)
+    # both sides take the attention oracle's lse (every row), rounded to fp32
+    _, lse64, st = oracle.attend(x["q"], x["k_cache"], x["v_cache"], x["k_draft"], x["v_draft"], x["parent"],
+                                 scale=x["scale"])
+    assert st == 0
+    lse32 = lse64.astype(np.float32).reshape(w.B, w.N, w.Hq)
+    heads = [3, 17]
+    score, status = ops.importance_scores(g["q"], g["k_cache"], torch.from_numpy(lse32).to(dev()),
+                                          torch.tensor(heads, dtype=torch.int32, device=dev()), scale=x["scale"])
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    lse32 = lse32.astype(np.float64)
+    toks = np.sort(np.random.default_rng(1).choice(w.L, 300, replace=False))
+    kc = x["k_cache"][:, :, toks].float().numpy()
+    want = oracle.importance_scores(x["q"].float().numpy(), kc, lse32, heads, scale=float(np.float32(x["scale"])))
+    got = score.cpu().numpy()[:, toks]
+    assert np.allclose(got, want, rtol=1e-4, atol=1e-7), np.abs(got - want).max()
