@@ -23,6 +23,7 @@ cores) on a bounded sample of rows of the same workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -380,6 +381,10 @@ def time_importance(dev, stream, args, peaks, peak_src, windows):
 
     w = W.workload(2)
     case = Case(w, dev)
+    # the call reads 67 MB, less than L2: flush before every call (the cache itself is larger,
+    # so the case has no flush of its own); the flush also keeps the host ahead of the device
+    case.flush = True
+    case.scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     _, lse = case.attend(case.g)
     heads = torch.tensor([3, 17], dtype=torch.int32, device=dev)
     score = torch.empty((w.B, w.L), dtype=torch.float32, device=dev)
@@ -399,9 +404,57 @@ def time_importance(dev, stream, args, peaks, peak_src, windows):
     e = {"workload": w.name + " importance scores, heads [3, 17]", "us_per_call": round(ms * 1e3, 2),
          "k_bytes": kbytes, "achieved_gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
          "kernel": "importance_tc (tcgen05: S^T = K Q^T per 128-token tile, TMEM lane per token)",
+         "l2": "flushed before every call (outside the events)",
          "peaks": f"{peak_src}: hbm {peaks['hbm_gbs']} GB/s", "calls_timed": len(v)}
     windows.append((e, t0, t1))
     case.release()
+    return e
+
+
+class _Flushed:
+    """A step function's inputs and the L2 flush before each call, for time_loop."""
+
+    def __init__(self, g, dev):
+        self.g = g
+        self.flush = True
+        self.scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def do_flush(self, i):
+        self.scratch.fill_(float(i))
+
+
+def time_lse_merge(dev, stream, args, peaks, peak_src, windows):
+    """The exported two-part log-sum-exp merge (spec_lse_merge) on 131,072 rows of d = 128:
+    reads two partials (o, lse) and writes one, 1,548 B a row, 203 MB a call."""
+    from speculative_decoding_verification_77_gb300 import ops
+
+    rows, d = 131072, 128
+    gen = torch.Generator().manual_seed(7)
+    g = {"o_a": torch.randn((rows, d), generator=gen).to(dev), "o_b": torch.randn((rows, d), generator=gen).to(dev),
+         "l_a": (4 * torch.randn((rows,), generator=gen)).to(dev), "l_b": (4 * torch.randn((rows,), generator=gen)).to(dev),
+         "out": torch.empty((rows, d), dtype=torch.float32, device=dev),
+         "lse": torch.empty((rows,), dtype=torch.float32, device=dev)}
+    fl = _Flushed(g, dev)
+
+    def run(t):
+        ops.lse_merge(t["o_a"], t["l_a"], t["o_b"], t["l_b"], out=t["out"], lse_out=t["lse"])
+
+    for _ in range(3):
+        run(g)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    v = time_loop(fl, run, stream, args.steps, args.extra_seconds / 4)
+    t1 = time.time()
+    ms = sum(v) / len(v)
+    nbytes = rows * (3 * d * 4 + 3 * 4)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    e = {"workload": f"lse_merge2 {rows} rows x d={d} (synthetic partials)", "us_per_call": round(ms * 1e3, 2),
+         "bytes": nbytes, "achieved_gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
+         "kernel": "lse_merge2 (one warp per row)", "l2": "flushed before every call (outside the events)",
+         "peaks": f"{peak_src}: hbm {peaks['hbm_gbs']} GB/s", "calls_timed": len(v)}
+    windows.append((e, t0, t1))
+    del g, fl
+    torch.cuda.empty_cache()
     return e
 
 
@@ -441,6 +494,8 @@ def run_native(args, ws_, rank, local):
     torch.cuda.set_device(dev)
     peaks, peak_src = measured_peaks()
     w = W.workload(args.workload, args.n)
+    if args.seq_len is not None:  # a shorter cache of the same layer (small profiling captures)
+        w = dataclasses.replace(w, L=args.seq_len, name=f"{w.name}@L{args.seq_len}")
     case = Case(w, dev, host_pinned=not args.no_e2e)
     stream = torch.cuda.current_stream(dev)
 
@@ -483,7 +538,8 @@ def run_native(args, ws_, rank, local):
     bastion = None
     windows = []
     if ws_ == 1 and args.extras != "none":
-        wanted = [int(c) for c in args.extras.split(",")] if args.extras != "all" else [1, 2, 3, 4, 5]
+        tokens = args.extras.split(",") if args.extras != "all" else ["1", "2", "3", "4", "5", "merge"]
+        wanted = [int(c) for c in tokens if c.isdigit()]
         sweep = []
         marginals = None
         for c in wanted:
@@ -502,8 +558,10 @@ def run_native(args, ws_, rank, local):
                 extras[wx.name] = e
                 cx.release()
                 del cx
-        if 2 in wanted:
+        if 2 in wanted or "importance" in tokens:
             extras["importance-scores-llama3-8b-layer"] = time_importance(dev, stream, args, peaks, peak_src, windows)
+        if "merge" in tokens:
+            extras["lse-merge2-131072-rows"] = time_lse_merge(dev, stream, args, peaks, peak_src, windows)
         if sweep and marginals is not None:
             head_e = None
             if w.tree == "best_first" and w.name.startswith("tree-sweep"):
@@ -678,6 +736,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", type=int, default=2)
     ap.add_argument("--n", type=int, default=None, help="draft-tree size of the tree-size sweep workload (5)")
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="cache length instead of the workload's own (small cases for ncu captures)")
     ap.add_argument("--extras", default="all",
                     help="other workloads timed in the same run at N=1: all, none, or a list like 1,3,4,5")
     ap.add_argument("--extra-seconds", type=float, default=1.0, help="device time per extra workload")

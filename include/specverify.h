@@ -204,6 +204,8 @@ spec_status_t spec_verify_attn_ex(const uint16_t *q, const uint16_t *k_cache, co
  * per row; two parts that both have lse = -inf give out = 0, lse = -inf.
  * o_a, o_b, out: fp32 [rows, d]; lse_a, lse_b, lse_out: fp32 [rows]; device.
  * out may alias o_a or o_b, lse_out may alias lse_a or lse_b (in place).
+ * rows <= 8 * (2^31 - 1) (one warp per row); d >= 1; pointers 4-byte aligned.
+ * SPEC_ERR_INVALID_ARG for null or misaligned pointers, rows or d out of range.
  */
 spec_status_t spec_lse_merge(const float *o_a, const float *lse_a, const float *o_b,
                              const float *lse_b, float *out, float *lse_out, int64_t rows, int d,

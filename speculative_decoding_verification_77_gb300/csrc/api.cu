@@ -294,7 +294,7 @@ spec_status_t spec_lse_merge(const float *o_a, const float *lse_a, const float *
     if (!aligned(o_a, 4) || !aligned(o_b, 4) || !aligned(out, 4) || !aligned(lse_a, 4) ||
         !aligned(lse_b, 4) || !aligned(lse_out, 4))
         return SPEC_ERR_INVALID_ARG;
-    if (rows > ((int64_t)1 << 36)) return SPEC_ERR_INVALID_ARG;
+    if (rows > (int64_t)INT32_MAX * 8) return SPEC_ERR_INVALID_ARG;  // one warp per row, 8 per block
     DeviceInfo dev;
     if (spec_status_t s = current_device(&dev)) return s;
     if (const cudaError_t e = launch_lse_merge2(o_a, lse_a, o_b, lse_b, out, lse_out, rows, d,

@@ -9,13 +9,16 @@
 // the thread that owns the lane sums its row's probabilities with no exchange.
 //
 // One CTA per (range of tiles, sequence): warp 0 streams the K tiles of the
-// listed heads' KV heads through a 4-slot ring by TMA (128-byte swizzle, the
-// layout the tensor core reads), warp 1 issues the MMAs (tile-major, head-minor)
-// into two TMEM accumulators, and warps 2-5 (TMEM lane quarters 2, 3, 0, 1) turn each
-// accumulator into probabilities and add them to their token's score. The
+// listed heads' KV heads through a ring of up to 6 slots by TMA (128-byte swizzle,
+// the layout the tensor core reads; as many slots as the shared memory left by the
+// queries holds), warp 1 issues the MMAs (tile-major, head-minor) into two TMEM
+// accumulators, and warps 2-9 turn each accumulator into probabilities and add them
+// to their token's score: two warps per TMEM lane quarter, each over half of the
+// queries, whose sums meet in shared memory at the tile's end. The
 // queries of every listed head and their lse (in base 2) are staged once per
-// CTA. Every wait is bounded; one that gives up records SPEC_ERR_TIMEOUT and the
-// CTA drains and returns.
+// CTA; thread 0 issues the queries' and the first ring's K loads as soon as the
+// barriers exist, so the rest of the set-up overlaps them. Every wait is bounded;
+// one that gives up records SPEC_ERR_TIMEOUT and the CTA drains and returns.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -28,37 +31,42 @@ namespace {
 using namespace sm100;
 
 constexpr int IT_T = 128;                // tokens per tile
-constexpr int IT_RING = 4;               // K tile slots
+constexpr int IT_RING_MAX = 6;           // K tile slots at most (the launch sizes the ring)
 constexpr int IT_SLOT = IT_T * kHeadDim * 2;  // 32 KiB
 constexpr int IT_MAX_ROWS = 256;         // listed heads x padded queries staged
-constexpr int IT_THREADS = 192;
+constexpr int IT_EPI_WARPS = 8;          // two per TMEM lane quarter, one per half of the queries
+constexpr int IT_THREADS = 64 + 32 * IT_EPI_WARPS;
 constexpr int IT_WARP_PRODUCER = 0, IT_WARP_MMA = 1, IT_WARP_EPI0 = 2;
 constexpr long long IT_WAIT_LIMIT = 4000000000LL;  // ~2 s
+constexpr int IT_SMEM_MAX = 232448;
 
 struct ItBars {
     uint64_t q_full;
-    uint64_t kv_full[IT_RING], kv_empty[IT_RING];
+    uint64_t kv_full[IT_RING_MAX], kv_empty[IT_RING_MAX];
     uint64_t acc_full[2], acc_empty[2];
     uint64_t mma_done;
     uint32_t tmem_base;
     uint32_t abort;
 };
-
-// smem: [Q rows: IT_MAX_ROWS x 256 B, two 64-column halves] [ring] [lse2: IT_MAX_ROWS floats] [bars]
-constexpr int IT_Q_BYTES = IT_MAX_ROWS * kHeadDim * 2;  // 64 KiB
-constexpr int IT_RING_OFF = IT_Q_BYTES;
-constexpr int IT_LSE_OFF = IT_RING_OFF + IT_RING * IT_SLOT;
-constexpr int IT_BAR_OFF = IT_LSE_OFF + IT_MAX_ROWS * 4;
-constexpr int IT_SMEM = IT_BAR_OFF + 256 + 1024;
 static_assert(sizeof(ItBars) <= 256, "barrier block");
-static_assert(IT_SMEM <= 232448, "fits one CTA");
+
+// smem (from a 1024-byte aligned base): [Q rows: nh*npad x 256 B, two 64-column halves,
+// rounded up to 1 KiB] [ring: `ring` slots of 32 KiB] [lse2: IT_MAX_ROWS floats]
+// [pair sums: 2 x IT_T floats] [bars]. The launch takes as many slots as fit.
+constexpr int IT_TAIL_BYTES = IT_MAX_ROWS * 4 + 2 * IT_T * 4 + 256;
 
 struct ItParams {
     int nh, npad;       // listed heads, queries per head padded to a multiple of 16
     int tiles_per_cta;  // cache tiles per CTA
+    int ring;           // K tile slots (<= IT_RING_MAX)
+    uint32_t q_bytes;   // the Q area (1 KiB multiple)
     uint32_t col_stride;  // TMEM columns per accumulator: npad rounded up to 32 (whole 32-column reads)
     uint32_t tmem_cols;
 };
+
+__host__ __device__ constexpr int it_smem_bytes(uint32_t q_bytes, int ring) {
+    return (int)q_bytes + ring * IT_SLOT + IT_TAIL_BYTES + 1024;  // + alignment slack
+}
 
 __device__ __forceinline__ bool it_wait(ItBars &bs, uint64_t *bar, uint32_t parity, int32_t *status) {
     if (*(volatile uint32_t *)&bs.abort) return false;
@@ -80,6 +88,30 @@ __device__ __forceinline__ void it_drain(uint64_t *bar, uint32_t parity) {
     }
 }
 
+// Every listed head's queries: rows b*N .. b*N + npad of head h, two column halves (one thread).
+__device__ __forceinline__ void it_load_q(ItBars &bs, uint8_t *sQ, const CUtensorMap *tm_q, const int32_t *heads,
+                                          const ItParams &ip, int Hq, int row0) {
+    mbar_arrive_expect_tx(&bs.q_full, (uint32_t)(ip.nh * ip.npad * kHeadDim * 2));
+    for (int j = 0; j < ip.nh; ++j) {
+        const int h = min(max(__ldg(heads + j), 0), Hq - 1);  // a bad head's rows are never used
+        for (int kh = 0; kh < 2; ++kh)
+            tma_load_3d(sQ + kh * (ip.nh * ip.npad * 128) + j * ip.npad * 128, tm_q, &bs.q_full, kh * 64, h, row0);
+    }
+}
+
+// Item n (tile tile0 + n / nh, listed head n % nh): the tile's 128 K rows of the head's KV
+// head into ring slot n % ring, whose previous use the caller has seen consumed (one thread).
+__device__ __forceinline__ void it_load_k(ItBars &bs, uint8_t *sRing, const CUtensorMap *tm_k, const int32_t *heads,
+                                          const ItParams &ip, int G, int Hq, int b, int tile0, int n) {
+    const int t = tile0 + n / ip.nh, j = n % ip.nh;
+    const int hk = min(max(__ldg(heads + j), 0), Hq - 1) / G;
+    const int slot = n % ip.ring;
+    uint8_t *dst = sRing + slot * IT_SLOT;
+    mbar_arrive_expect_tx(&bs.kv_full[slot], IT_SLOT);
+    tma_load_4d(dst, tm_k, &bs.kv_full[slot], 0, t * IT_T, hk, b);
+    tma_load_4d(dst + IT_SLOT / 2, tm_k, &bs.kv_full[slot], 64, t * IT_T, hk, b);
+}
+
 __global__ void __launch_bounds__(IT_THREADS, 1)
 importance_tc_kernel(const float *__restrict__ lse, const int32_t *__restrict__ heads, int N, int Hq, int Hkv,
                      int L, const int32_t *__restrict__ ctx_lens, float scale, float *__restrict__ score, int64_t ld,
@@ -87,10 +119,12 @@ importance_tc_kernel(const float *__restrict__ lse, const int32_t *__restrict__ 
                      const __grid_constant__ CUtensorMap tm_k) {
     extern __shared__ uint8_t it_raw[];
     uint8_t *smem = it_raw + ((1024 - (smem_u32(it_raw) & 1023)) & 1023);
+    const int ring = ip.ring;
     uint8_t *sQ = smem;
-    uint8_t *sRing = smem + IT_RING_OFF;
-    float *sLse2 = reinterpret_cast<float *>(smem + IT_LSE_OFF);
-    ItBars &bs = *reinterpret_cast<ItBars *>(smem + IT_BAR_OFF);
+    uint8_t *sRing = smem + ip.q_bytes;
+    float *sLse2 = reinterpret_cast<float *>(sRing + ring * IT_SLOT);
+    float *sPair = sLse2 + IT_MAX_ROWS;  // [tile parity][token of the tile]
+    ItBars &bs = *reinterpret_cast<ItBars *>(sPair + 2 * IT_T);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.y;
     const int G = Hq / Hkv;
@@ -106,17 +140,25 @@ importance_tc_kernel(const float *__restrict__ lse, const int32_t *__restrict__ 
 
     if (threadIdx.x == 0) {
         mbar_init(&bs.q_full, 1);
-        for (int i = 0; i < IT_RING; ++i) {
+        for (int i = 0; i < ring; ++i) {
             mbar_init(&bs.kv_full[i], 1);
             mbar_init(&bs.kv_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bs.acc_full[i], 1);
-            mbar_init(&bs.acc_empty[i], 4);
+            mbar_init(&bs.acc_empty[i], IT_EPI_WARPS);
         }
         mbar_init(&bs.mma_done, 1);
         bs.abort = 0;
         fence_mbar_init();
+        // the queries and the ring's first K tiles go out before the rest of the set-up
+        // (the lse staging's loads, the TMEM allocation), which then overlaps them
+        if (nitems > 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            it_load_q(bs, sQ, &tm_q, heads, ip, Hq, b * N);
+            for (int n = 0; n < nitems && n < ring; ++n) it_load_k(bs, sRing, &tm_k, heads, ip, G, Hq, b, tile0, n);
+        }
     }
     // lse of every listed head's queries, in base 2; rows past N, or whose lse is -inf or
     // NaN (nothing attended), get +inf so that they add exp2(-inf) = 0
@@ -142,30 +184,15 @@ importance_tc_kernel(const float *__restrict__ lse, const int32_t *__restrict__ 
 
     if (warp == IT_WARP_PRODUCER) {
         if (lane == 0 && nitems > 0) {
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_k);
-            // every listed head's queries: rows b*N .. b*N + npad of head h, two column halves
-            mbar_arrive_expect_tx(&bs.q_full, (uint32_t)(ip.nh * ip.npad * kHeadDim * 2));
-            for (int j = 0; j < ip.nh; ++j) {
-                const int h = min(max(__ldg(heads + j), 0), Hq - 1);  // a bad head's rows are never used
-                for (int kh = 0; kh < 2; ++kh)
-                    tma_load_3d(sQ + kh * (ip.nh * ip.npad * 128) + j * ip.npad * 128, &tm_q, &bs.q_full, kh * 64, h,
-                                b * N);
-            }
+            // the queries and items 0 .. ring-1 were issued at the start
             bool ok = true;
-            for (int n = 0; ok && n < nitems; ++n) {
-                const int t = tile0 + n / ip.nh, j = n % ip.nh;
-                const int hk = min(max(__ldg(heads + j), 0), Hq - 1) / G;
-                const int slot = n % IT_RING;
-                if (n >= IT_RING && !(ok = it_wait(bs, &bs.kv_empty[slot], ((n / IT_RING) - 1) & 1, status))) break;
-                uint8_t *dst = sRing + slot * IT_SLOT;
-                mbar_arrive_expect_tx(&bs.kv_full[slot], IT_SLOT);
-                tma_load_4d(dst, &tm_k, &bs.kv_full[slot], 0, t * IT_T, hk, b);
-                tma_load_4d(dst + IT_SLOT / 2, &tm_k, &bs.kv_full[slot], 64, t * IT_T, hk, b);
+            for (int n = ring; ok && n < nitems; ++n) {
+                if (!(ok = it_wait(bs, &bs.kv_empty[n % ring], ((n / ring) - 1) & 1, status))) break;
+                it_load_k(bs, sRing, &tm_k, heads, ip, G, Hq, b, tile0, n);
             }
             // drain the copies still in flight
-            for (int n = nitems > IT_RING ? nitems - IT_RING : 0; n < nitems; ++n)
-                it_drain(&bs.kv_full[n % IT_RING], (n / IT_RING) & 1);
+            for (int n = nitems > ring ? nitems - ring : 0; n < nitems; ++n)
+                it_drain(&bs.kv_full[n % ring], (n / ring) & 1);
             it_drain(&bs.q_full, 0);
         }
         __syncwarp();
@@ -176,8 +203,8 @@ importance_tc_kernel(const float *__restrict__ lse, const int32_t *__restrict__ 
         const uint64_t dk0 = desc_sw128(smem_u32(sRing), 16, 1024);
         const uint32_t qhalf = (uint32_t)(ip.nh * ip.npad * 128);  // bytes to the second column half
         for (int n = 0; ok && n < nitems; ++n) {
-            const int j = n % ip.nh, slot = n % IT_RING, buf = n & 1;
-            if (!(ok = __all_sync(0xffffffffu, it_wait(bs, &bs.kv_full[slot], (n / IT_RING) & 1, status)))) break;
+            const int j = n % ip.nh, slot = n % ring, buf = n & 1;
+            if (!(ok = __all_sync(0xffffffffu, it_wait(bs, &bs.kv_full[slot], (n / ring) & 1, status)))) break;
             if (n >= 2 && !(ok = __all_sync(0xffffffffu, it_wait(bs, &bs.acc_empty[buf], ((n >> 1) - 1) & 1, status))))
                 break;
             tc_fence_after();
@@ -195,8 +222,10 @@ importance_tc_kernel(const float *__restrict__ lse, const int32_t *__restrict__ 
         it_drain(&bs.mma_done, 0);
     } else {
         // epilogue: a warp may only read the TMEM lane quarter of its index mod 4, so warp w
-        // takes lanes 32 (w & 3) .. + 31 = those tokens of the tile
-        const int lg = warp & 3;
+        // takes lanes 32 (w & 3) .. + 31 = those tokens of the tile; warps 2-5 take the query
+        // columns [0, 32) + 64 k, warps 6-9 [32, 64) + 64 k, and at the tile's end the second
+        // half hands its sums to the first through shared memory
+        const int lg = warp & 3, half = (warp - IT_WARP_EPI0) >> 2;
         const uint32_t lane_addr = (uint32_t)(lg * 32) << 16;
         const float sl2 = scale * 1.4426950408889634f;
         bool ok = true;
@@ -207,7 +236,7 @@ importance_tc_kernel(const float *__restrict__ lse, const int32_t *__restrict__ 
             tc_fence_after();
             if (ok) {
                 const float *l2 = sLse2 + j * ip.npad;
-                for (int c0 = 0; c0 < N; c0 += 32) {
+                for (int c0 = 32 * half; c0 < N; c0 += 64) {
                     uint32_t r[32];
                     tmem_ld32(tmem + lane_addr + (uint32_t)buf * ip.col_stride + (uint32_t)c0, r);
                     tmem_wait_ld();
@@ -221,8 +250,16 @@ importance_tc_kernel(const float *__restrict__ lse, const int32_t *__restrict__ 
             __syncwarp();
             if (lane == 0) mbar_arrive(&bs.acc_empty[buf]);
             if (j == ip.nh - 1) {  // the tile's last head: its tokens' scores are complete
-                const int t = (tile0 + n / ip.nh) * IT_T + lg * 32 + lane;
-                if (t < L) score[(int64_t)b * ld + t] = (ok && t < n_ctx) ? acc : 0.f;
+                const int tl = n / ip.nh;
+                float *pair = sPair + (tl & 1) * IT_T + lg * 32 + lane;
+                if (half) *pair = acc;
+                // the 8 epilogue warps; a buffer is rewritten two tiles later, after the next
+                // barrier, which its reader has passed only once it has read it
+                asm volatile("bar.sync 1, %0;" ::"n"(32 * IT_EPI_WARPS) : "memory");
+                if (!half) {
+                    const int t = (tile0 + tl) * IT_T + lg * 32 + lane;
+                    if (t < L) score[(int64_t)b * ld + t] = (ok && t < n_ctx) ? acc + *pair : 0.f;
+                }
                 acc = 0.f;
             }
         }
@@ -279,11 +316,13 @@ bool launch_importance_tc(const __nv_bfloat16 *q, const __nv_bfloat16 *k_cache, 
         if (!it_encode(&mk, k_cache, 4, dims, strides, box)) return false;
     }
     static PerDeviceOnce attr_once;
-    *err = once_per_device(attr_once, [] { return kernel_attributes(importance_tc_kernel, IT_SMEM); });
+    *err = once_per_device(attr_once, [] { return kernel_attributes(importance_tc_kernel, IT_SMEM_MAX); });
     if (*err != cudaSuccess) return true;
     ItParams ip;
     ip.nh = nh;
     ip.npad = npad;
+    ip.q_bytes = (uint32_t)((nh * npad * kHeadDim * 2 + 1023) / 1024 * 1024);
+    ip.ring = std::min(IT_RING_MAX, (int)((IT_SMEM_MAX - it_smem_bytes(ip.q_bytes, 0)) / IT_SLOT));
     const int ntiles = (L + IT_T - 1) / IT_T;
     // about one CTA per SM over the whole batch
     const int ctas_per_seq = std::max(1, std::min(ntiles, (sms + B - 1) / B));
@@ -292,7 +331,7 @@ bool launch_importance_tc(const __nv_bfloat16 *q, const __nv_bfloat16 *k_cache, 
     ip.tmem_cols = 32;
     while (ip.tmem_cols < 2 * ip.col_stride) ip.tmem_cols <<= 1;
     const dim3 grid((unsigned)((ntiles + ip.tiles_per_cta - 1) / ip.tiles_per_cta), (unsigned)B);
-    importance_tc_kernel<<<grid, IT_THREADS, IT_SMEM, s>>>(lse, heads, N, Hq, Hkv, L, ctx_lens, scale, score, ld,
+    importance_tc_kernel<<<grid, IT_THREADS, it_smem_bytes(ip.q_bytes, ip.ring), s>>>(lse, heads, N, Hq, Hkv, L, ctx_lens, scale, score, ld,
                                                           status, ip, mq, mk);
     count_launches(1);
     *err = cudaGetLastError();

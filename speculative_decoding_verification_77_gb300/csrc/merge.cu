@@ -271,7 +271,13 @@ __global__ void __launch_bounds__(256) merge_tree_kernel(VerifyArgs a, SplitPlan
     }
 }
 
-// Exported two-part merge: one warp per row, any d.
+// Exported two-part merge: one warp per row, any d. With VEC (d a multiple of 4, every
+// row 16-byte aligned) a lane moves 4 consecutive floats per load and store, so a row of
+// d = 128 is one float4 per lane and part; the two lse loads and the first row loads are
+// issued together. In place (out == o_a, lse_out == lse_a) is allowed: every lane reads its
+// own elements before writing them, and the lse values are read by all lanes before lane 0
+// writes the row's lse.
+template <bool VEC>
 __global__ void __launch_bounds__(256) lse_merge2_kernel(const float *o_a, const float *lse_a,
                                                          const float *o_b, const float *lse_b,
                                                          float *out, float *lse_out, int64_t rows,
@@ -280,6 +286,13 @@ __global__ void __launch_bounds__(256) lse_merge2_kernel(const float *o_a, const
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
     const float la = lse_a[row], lb = lse_b[row];
+    const float *pa = o_a + row * d, *pb = o_b + row * d;
+    float *po = out + row * d;
+    float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), y0 = x0;
+    if (VEC && 4 * lane < d) {  // the first float4 of each part, in flight with the lse loads
+        x0 = *reinterpret_cast<const float4 *>(pa + 4 * lane);
+        y0 = *reinterpret_cast<const float4 *>(pb + 4 * lane);
+    }
     __syncwarp();  // every lane has read the lse values before lane 0 may overwrite them in place
     const float m = fmaxf(la, lb);
     float wa = 0.f, wb = 0.f, l = -INFINITY;
@@ -291,11 +304,18 @@ __global__ void __launch_bounds__(256) lse_merge2_kernel(const float *o_a, const
         l = m + __logf(ea + eb);
     }
     if (isnan(la) || isnan(lb)) { wa = wb = l = NAN; }
-    const float *pa = o_a + row * d, *pb = o_b + row * d;
-    float *po = out + row * d;
-    for (int c = lane; c < d; c += 32) {
-        const float x = pa[c], y = pb[c];
-        po[c] = (wa == 0.f ? 0.f : wa * x) + (wb == 0.f ? 0.f : wb * y);
+    auto mix = [&](float x, float y) { return (wa == 0.f ? 0.f : wa * x) + (wb == 0.f ? 0.f : wb * y); };
+    if (VEC) {
+        for (int c = 4 * lane; c < d; c += 128) {
+            float4 x = x0, y = y0;
+            if (c != 4 * lane) {
+                x = *reinterpret_cast<const float4 *>(pa + c);
+                y = *reinterpret_cast<const float4 *>(pb + c);
+            }
+            *reinterpret_cast<float4 *>(po + c) = make_float4(mix(x.x, y.x), mix(x.y, y.y), mix(x.z, y.z), mix(x.w, y.w));
+        }
+    } else {
+        for (int c = lane; c < d; c += 32) po[c] = mix(pa[c], pb[c]);
     }
     if (lane == 0) lse_out[row] = l;
 }
@@ -312,7 +332,8 @@ cudaError_t merge_attributes() {
         if (r == cudaSuccess) r = kernel_attributes(merge_tree_kernel<4>, kMaxMergeSmem);
         if (r == cudaSuccess) r = kernel_attributes(merge_tree_kernel<2>, kMaxMergeSmem);
         if (r == cudaSuccess) r = kernel_attributes(merge_tree_kernel<1>, kMaxMergeSmem);
-        if (r == cudaSuccess) r = kernel_attributes(lse_merge2_kernel, 0);
+        if (r == cudaSuccess) r = kernel_attributes(lse_merge2_kernel<true>, 0);
+        if (r == cudaSuccess) r = kernel_attributes(lse_merge2_kernel<false>, 0);
         return r;
     });
 }
@@ -354,7 +375,12 @@ cudaError_t launch_lse_merge2(const float *o_a, const float *lse_a, const float 
     if (rows == 0) return cudaSuccess;
     if (const cudaError_t e = merge_attributes(); e != cudaSuccess) return e;
     const int64_t blocks = (rows * 32 + 255) / 256;
-    lse_merge2_kernel<<<(unsigned)blocks, 256, 0, s>>>(o_a, lse_a, o_b, lse_b, out, lse_out, rows, d);
+    const bool vec = d % 4 == 0 && ((reinterpret_cast<uintptr_t>(o_a) | reinterpret_cast<uintptr_t>(o_b) |
+                                     reinterpret_cast<uintptr_t>(out)) & 15) == 0;
+    if (vec)
+        lse_merge2_kernel<true><<<(unsigned)blocks, 256, 0, s>>>(o_a, lse_a, o_b, lse_b, out, lse_out, rows, d);
+    else
+        lse_merge2_kernel<false><<<(unsigned)blocks, 256, 0, s>>>(o_a, lse_a, o_b, lse_b, out, lse_out, rows, d);
     count_launches(1);
     return cudaGetLastError();
 }

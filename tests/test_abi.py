@@ -158,6 +158,7 @@ def test_merge_rejects_bad_arguments_on_the_host(lib):
     assert lib.spec_lse_merge(None, 4, 4, 4, 4, 4, 10, 128, None) == 1
     assert lib.spec_lse_merge(4, 4, 4, 4, 4, 4, -1, 128, None) == 1
     assert lib.spec_lse_merge(4, 4, 4, 4, 4, 4, 10, 0, None) == 1
+    assert lib.spec_lse_merge(4, 4, 4, 4, 4, 4, 8 * (2**31 - 1) + 1, 128, None) == 1  # past the grid's reach
 
 
 def test_package_import_loads_nothing():

@@ -180,6 +180,16 @@ def test_row_groups_and_head_ratios(ops, N, Hq, Hkv):
     run_dense(ops, x, to_dev(x))
 
 
+# Up to 256 nodes the speculative part runs as its own small-block grid beside the cache
+# kernel (parents held in registers, 32 a register); above that the merge walks the tree
+# itself. Chains put the deepest walks on both sides of that bound, with G = 8 (two warps
+# of four heads per node in the separate grid) and G = 3 (one head per warp).
+@pytest.mark.parametrize("N,Hq,Hkv", [(256, 16, 2), (257, 8, 2), (256, 6, 2), (255, 4, 4)])
+def test_deep_chains_both_tree_paths(ops, N, Hq, Hkv):
+    x = small(31 + N, B=2, N=N, Hq=Hq, Hkv=Hkv, L=700, tree="chain")
+    run_dense(ops, x, to_dev(x))
+
+
 def test_cache_only_then_merge_equals_full(ops):
     x = small(21, L=900)
     g = to_dev(x)
@@ -201,8 +211,10 @@ def test_cache_only_then_merge_equals_full(ops):
     np.testing.assert_allclose(ml.cpu().numpy().reshape(-1), ml_ref, atol=1e-5, rtol=0)
 
 
-def test_lse_merge_special_rows_and_in_place(ops):
-    rows, d = 1000, 128
+# d = 128: one float4 per lane; 256: two; 36: lanes past d idle; 70: the scalar form
+@pytest.mark.parametrize("d", [128, 256, 36, 70])
+def test_lse_merge_special_rows_and_in_place(ops, d):
+    rows = 1000
     gen = torch.Generator().manual_seed(3)
     oa = torch.randn(rows, d, generator=gen)
     ob = torch.randn(rows, d, generator=gen)
