@@ -51,8 +51,17 @@ SWEEP_N = (1, 4, 16, 64, 256)
 # capture, keyed by the sha256 of the kernel sources it was taken on and the
 # workload; a changed kernel reports null.
 NCU_TRAFFIC = {
-    ("cdb83f410f5b09e1", "llama3-8b-layer-B4-L32k-N64-tree"): 540_644_864 + 8_498_432,
-    ("cdb83f410f5b09e1", "sparse-hybrid-B16-L32k-k2048-N8-chain"): 136_158_464 + 6_797_824,
+    ("68eecf5f6cb9cb11", "llama3-8b-layer-B4-L32k-N64-tree"): 540_649_728 + 8_762_368,
+    ("68eecf5f6cb9cb11", "sparse-hybrid-B16-L32k-k2048-N8-chain"): 136_131_072 + 6_466_560,
+    # captured at L = 32k (1.08 GB of reads, 12.6 MB of partials written): reads scaled by 4
+    ("68eecf5f6cb9cb11", "qwen2.5-72b-layer-B8-L128k-N32-tree"): 4 * 1_081_532_000 + 12_563_968,
+    ("68eecf5f6cb9cb11", "tree-sweep-B8-L16k-N256-best-first"): 2_173_974_000 + 39_198_720,
+}
+NCU_TRAFFIC_NOTE = {
+    "qwen2.5-72b-layer-B8-L128k-N32-tree": "from an ncu capture at L=32k: K/V reads x4 (they grow with L), "
+                                           "partial writes as captured (they do not)",
+    "tree-sweep-B8-L16k-N256-best-first": "4.1x the algorithmic bytes: G*N = 1024 rows per KV head make four "
+                                          "256-row units, each streaming the whole K/V of its head",
 }
 
 
@@ -335,6 +344,10 @@ def roofline_entry(w, kernel_ms, peaks, peak_src):
          "frac_bound": round((t_tc if bound == "tensor" else t_hbm) / (kernel_ms * 1e-3), 4),
          "traffic": NCU_TRAFFIC.get((kernel_source_hash(), w.name)),
          "peaks": f"{peak_src}: hbm {peaks['hbm_gbs']} GB/s, bf16 sustained {peaks['bf16_tflops_sustained']} TFLOP/s"}
+    if r["traffic"] is not None:
+        r["traffic_over_algorithmic"] = round(r["traffic"] / kv, 3)
+        if w.name in NCU_TRAFFIC_NOTE:
+            r["traffic_note"] = NCU_TRAFFIC_NOTE[w.name]
     return r
 
 

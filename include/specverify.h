@@ -223,7 +223,8 @@ spec_status_t spec_lse_merge(const float *o_a, const float *lse_a, const float *
  * for spec_verify_attn; lse [B, N, Hq] fp32 as spec_verify_attn returns it
  * (rows with lse = -inf add nothing). score: fp32 device, ld >= L. A head
  * index outside [0, Hq) adds nothing and sets SPEC_ERR_BAD_INPUT in *status
- * (device int32, zeroed by the call first; may be NULL).
+ * (device int32, written whole by the call: SPEC_OK, or SPEC_ERR_BAD_INPUT for a
+ * listed head outside [0, Hq), or SPEC_ERR_TIMEOUT; may be NULL).
  * Requires d == 128 and N <= 512 (else SPEC_ERR_UNSUPPORTED), 1 <= B <= 65535,
  * Hq % Hkv == 0, 16-byte aligned q and cache.
  */

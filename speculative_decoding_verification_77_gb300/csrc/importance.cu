@@ -110,12 +110,7 @@ extern "C" spec_status_t spec_importance_scores(const uint16_t *q, const uint16_
     if (!(scale == scale)) return SPEC_ERR_INVALID_ARG;
     if (d != kHeadDim || N > kImpMaxN) return SPEC_ERR_UNSUPPORTED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (status) {
-        if (const cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), s); e != cudaSuccess)
-            return (spec_status_t)cuda_failure(e);
-    }
-    if (L == 0) return SPEC_OK;
-    if (nh > 0) {  // the tensor-core form where the shape allows it
+    if (L > 0 && nh > 0) {  // the tensor-core form where the shape allows it (it writes the status word)
         int dev = 0, sms = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return (spec_status_t)cuda_failure(cudaGetLastError());
@@ -125,6 +120,11 @@ extern "C" spec_status_t spec_importance_scores(const uint16_t *q, const uint16_
                                  score, ld, status, sms, s, &e))
             return e == cudaSuccess ? SPEC_OK : (spec_status_t)cuda_failure(e);
     }
+    if (status) {
+        if (const cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), s); e != cudaSuccess)
+            return (spec_status_t)cuda_failure(e);
+    }
+    if (L == 0) return SPEC_OK;
     const size_t smem = (size_t)N * 256 + (size_t)N * sizeof(float);
     static PerDeviceOnce attr_once;
     const cudaError_t attr = once_per_device(

@@ -170,8 +170,19 @@ importance_tc_kernel(const float *__restrict__ lse, const int32_t *__restrict__ 
             const float l = __ldg(lse + ((int64_t)b * N + i) * Hq + h);
             if (l > -INFINITY) v = l * 1.4426950408889634f;
         }
-        if (i == 0 && (h < 0 || h >= Hq) && status) atomicMax(status, (int32_t)SPEC_ERR_BAD_INPUT);  // adds nothing
         sLse2[r] = v;
+    }
+    // the status word, written whole by the first CTA (no clearing memset before the launch):
+    // SPEC_ERR_BAD_INPUT if a listed head is outside [0, Hq) (its rows add nothing), else
+    // SPEC_OK; a wait that gives up later raises it to SPEC_ERR_TIMEOUT
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < 32) {
+        bool bad = false;
+        for (int j = threadIdx.x; j < ip.nh; j += 32) {
+            const int h = __ldg(heads + j);
+            bad |= h < 0 || h >= Hq;
+        }
+        bad = __any_sync(0xffffffffu, bad);
+        if (threadIdx.x == 0 && status) *status = bad ? (int32_t)SPEC_ERR_BAD_INPUT : (int32_t)SPEC_OK;
     }
     if (warp == IT_WARP_PRODUCER) {
         tmem_alloc(&bs.tmem_base, ip.tmem_cols);

@@ -350,7 +350,7 @@ def accept_commit(draft_token, parent, target_next, k_cache=None, v_cache=None, 
     return path, length, bonus, status
 
 
-def importance_scores(q, k_cache, lse, heads, *, scale=None, ctx_lens=None, out=None):
+def importance_scores(q, k_cache, lse, heads, *, scale=None, ctx_lens=None, out=None, status=None):
     """Target-historical importance of every cache token on the given query heads.
 
     q [B,N,Hq,d] bf16, k_cache [B,Hkv,L,d] bf16 (d contiguous), lse fp32 [B,N,Hq] (from verify_attn),
@@ -372,7 +372,9 @@ def importance_scores(q, k_cache, lse, heads, *, scale=None, ctx_lens=None, out=
         scale = 1.0 / math.sqrt(d)
     if out is None:
         out = torch.empty((B, L), dtype=torch.float32, device=q.device)
-    status = torch.empty((1,), dtype=torch.int32, device=q.device)
+    if status is None:
+        status = torch.empty((1,), dtype=torch.int32, device=q.device)
+    _need(status, torch.int32, "status", 1)
     _check("spec_importance_scores", lib.spec_importance_scores(
         _ptr(q), _ptr(k_cache), k_cache.stride(0), k_cache.stride(1), k_cache.stride(2), _ptr(lse), _ptr(heads),
         heads.numel(), B, N, Hq, Hkv, d, L, _ptr(ctx_lens), float(scale), _ptr(out), out.stride(0), _ptr(status),

@@ -592,9 +592,10 @@ def test_importance_scores_match_oracle(ops, case):
     want = oracle.importance_scores(x["q"].float().numpy(), x["k_cache"].float().numpy(), lse32.astype(np.float64),
                                     valid, scale=float(np.float32(x["scale"])), ctx_lens=ctx)
     g = to_dev(x)
+    stale = torch.full((1,), 7, dtype=torch.int32, device=dev())  # the call must write the word whole
     score, status = ops.importance_scores(g["q"], g["k_cache"], torch.from_numpy(lse32).to(dev()),
                                           torch.tensor(heads, dtype=torch.int32, device=dev()), scale=x["scale"],
-                                          ctx_lens=torch.from_numpy(ctx).to(dev()))
+                                          ctx_lens=torch.from_numpy(ctx).to(dev()), status=stale)
     torch.cuda.synchronize()
     got = score.cpu().numpy()
     assert int(status.item()) == (5 if case == "bad_head" else 0)
