@@ -83,6 +83,14 @@ def load_library(path: str):
                                         ctypes.c_int, ctypes.c_int, P, ctypes.c_float,
                                         P, ctypes.c_int64, P, P]
     lib.oracle_attend_paged.restype = ctypes.c_int
+    lib.oracle_attend_fp8.argtypes = [P, P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, P, P,
+                                      P, P, P, P, ctypes.c_int,
+                                      ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_int, ctypes.c_int, P, ctypes.c_float,
+                                      P, ctypes.c_int64, P, P]
+    lib.oracle_attend_fp8.restype = ctypes.c_int
+    lib.oracle_e4m3_value.argtypes = [ctypes.c_int]
+    lib.oracle_e4m3_value.restype = ctypes.c_double
     lib.oracle_lse_merge.argtypes = [P, P, P, P, ctypes.c_int64, ctypes.c_int, P, P]
     lib.oracle_lse_merge.restype = ctypes.c_int
     return lib
@@ -99,6 +107,8 @@ def _np(t, dtype):
         t = t.detach().cpu().contiguous()
         if t.dtype == torch.bfloat16:
             return t.view(torch.int16).numpy().view(np.uint16)
+        if t.dtype == torch.float8_e4m3fn:  # the 8-bit codes themselves
+            return t.view(torch.uint8).numpy()
         t = t.numpy()
     return np.ascontiguousarray(t, dtype=dtype)
 
@@ -194,6 +204,45 @@ def attend_paged(q, k_pool, v_pool, k_draft, v_draft, parent, block_table, *, L:
     if st == 1:
         raise ValueError("oracle_attend_paged: invalid argument")
     return out, lse, st
+
+
+def attend_fp8(q, k_codes, v_codes, k_scale, v_scale, k_draft, v_draft, parent, *, scale: float,
+               ctx_lens=None, idx=None, rows=None):
+    """attend() over a cache stored as 8-bit floats (a layout the pages do not use): K and V
+    [B, Hkv, L, d] E4M3 codes (uint8, or torch float8_e4m3fn), the value of a code being the
+    OCP E4M3 number it encodes times k_scale[b, h] (v_scale[b, h]), fp32 [B, Hkv]. Queries and
+    the draft block are bf16 as in attend(). Returns (out float64 [n_rows, d], lse, status)."""
+    qn = _np(q, np.uint16)
+    B, N, Hq, d = qn.shape
+    kc = _np(k_codes, np.uint8)
+    vc = _np(v_codes, np.uint8)
+    _, Hkv, L, _ = kc.shape
+    ks = _np(k_scale, np.float32)
+    vs = _np(v_scale, np.float32)
+    assert ks.shape == (B, Hkv) and vs.shape == (B, Hkv)
+    kd = _np(k_draft, np.uint16)
+    vd = _np(v_draft, np.uint16)
+    par = _np(parent, np.int32)
+    ix = _np(idx, np.int32)
+    budget = 0 if ix is None else ix.shape[1]
+    cl = _np(ctx_lens, np.int32)
+    if rows is None:
+        rows = np.arange(B * N * Hq, dtype=np.int64)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty((rows.shape[0], d), dtype=np.float64)
+    lse = np.empty((rows.shape[0],), dtype=np.float64)
+    st = _load().oracle_attend_fp8(_ptr(qn), _ptr(kc), _ptr(vc), Hkv * L * d, L * d, d, _ptr(ks), _ptr(vs),
+                                   _ptr(kd), _ptr(vd), _ptr(par), _ptr(ix), budget, B, N, Hq, Hkv, d, L,
+                                   _ptr(cl), ctypes.c_float(scale), _ptr(rows), rows.shape[0], _ptr(out),
+                                   _ptr(lse))
+    if st == 1:
+        raise ValueError("oracle_attend_fp8: invalid argument")
+    return out, lse, st
+
+
+def e4m3_value(code: int) -> float:
+    """The number an E4M3 code (0..255) stands for (NaN for the two NaN codes)."""
+    return float(_load().oracle_e4m3_value(int(code)))
 
 
 def lse_merge(o_a, lse_a, o_b, lse_b):

@@ -34,6 +34,13 @@
  *                   a per-sequence block table). A block entry outside the pool
  *                   hides its tokens and is reported as bad input.
  *
+ *   oracle_attend_fp8  oracle_attend over a cache stored as 8-bit floats (not on
+ *                   the pages): each K (V) element is an E4M3 code of the OCP 8-bit
+ *                   floating-point formats (1 sign bit, 4 exponent bits with bias 7,
+ *                   3 mantissa bits; subnormals; no infinities; S.1111.111 is NaN),
+ *                   and the cache value is that number times a scale per (sequence,
+ *                   KV head), one for K and one for V. The draft block stays bf16.
+ *
  * Readings where the pages are silent (also listed in the design notes):
  *   - score comparison: larger is better; -0 == +0; NaN ranks below every
  *     number (including -inf) and NaNs tie; ties go to the lower index.
@@ -68,6 +75,17 @@ static double bf16_to_double(uint16_t h)
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* E4M3 code -> exact double (OCP 8-bit floating point, E4M3):
+   exponent field 0: (-1)^s * m/8 * 2^(1-7); 1..15: (-1)^s * (1 + m/8) * 2^(e-7);
+   exponent 15 with mantissa 7 is NaN (the format has no infinities). */
+static double e4m3_to_double(uint8_t x)
+{
+    int sgn = x >> 7, e = (x >> 3) & 15, m = x & 7;
+    if (e == 15 && m == 7) return NAN;
+    double v = e == 0 ? ldexp((double)m / 8.0, 1 - 7) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sgn ? -v : v;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -175,7 +193,17 @@ typedef struct {
     int64_t table_ld;
     int block_size;
     int64_t num_blocks;
+    /* element format: 0 = bf16; 1 = E4M3 codes, value = code * scale[b * Hkv + h] */
+    int fp8;
+    const float *k_scale, *v_scale;
 } cache_layout;
+
+/* Element c of the cache row at element offset off (K or V), as the exact double it stands for. */
+static double cache_value(const cache_layout *cl, const void *base, const float *scale_bh, int64_t off, int c)
+{
+    if (!cl->fp8) return bf16_to_double(((const uint16_t *)base)[off + c]);
+    return e4m3_to_double(((const uint8_t *)base)[off + c]) * (double)*scale_bh;
+}
 
 /* Element offset of the row of token t (sequence b, KV head hk); 0 when the row does not
    exist (a block entry outside [0, num_blocks)), else 1. */
@@ -191,7 +219,7 @@ static int cache_row(const cache_layout *cl, int b, int hk, int64_t t, int64_t *
     return 1;
 }
 
-static int attend_core(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+static int attend_core(const uint16_t *q, const void *k_cache, const void *v_cache,
                        const cache_layout *cl, const uint16_t *k_draft, const uint16_t *v_draft,
                        const int32_t *parent, const int32_t *idx, int budget, int B, int N, int Hq,
                        int Hkv, int d, int L, const int32_t *ctx_lens, float scale, int64_t cache_begin,
@@ -199,6 +227,7 @@ static int attend_core(const uint16_t *q, const uint16_t *k_cache, const uint16_
 {
     if (B < 1 || N < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || d < 1 || L < 0 || !q || !out ||
         !lse || !rows || (L > 0 && (!k_cache || !v_cache)) || (idx && budget < 0) ||
+        (cl->fp8 && L > 0 && (!cl->k_scale || !cl->v_scale)) ||
         ((k_draft == NULL) != (v_draft == NULL)) || (k_draft && !parent))
         return ORACLE_INVALID_ARG;
     const int G = Hq / Hkv;
@@ -265,16 +294,18 @@ static int attend_core(const uint16_t *q, const uint16_t *k_cache, const uint16_
         }
 
         /* scores over all visible keys */
+        const float *ks = cl->fp8 ? cl->k_scale + (int64_t)b * Hkv + hk : NULL;
+        const float *vs = cl->fp8 ? cl->v_scale + (int64_t)b * Hkv + hk : NULL;
         double mx = -INFINITY;
         for (int64_t j = 0; j < nkeys; ++j) {
             if (!visible[j]) continue;
-            const uint16_t *krow;
-            if (j < ncache_cand)
-                krow = k_cache + coff[j];
-            else
-                krow = k_draft + (((int64_t)b * N + (j - ncache_cand)) * Hkv + hk) * d;
             double dot = 0.0;
-            for (int c = 0; c < d; ++c) dot += bf16_to_double(qrow[c]) * bf16_to_double(krow[c]);
+            if (j < ncache_cand) {
+                for (int c = 0; c < d; ++c) dot += bf16_to_double(qrow[c]) * cache_value(cl, k_cache, ks, coff[j], c);
+            } else {
+                const uint16_t *krow = k_draft + (((int64_t)b * N + (j - ncache_cand)) * Hkv + hk) * d;
+                for (int c = 0; c < d; ++c) dot += bf16_to_double(qrow[c]) * bf16_to_double(krow[c]);
+            }
             s[j] = sc * dot;
             if (s[j] > mx) mx = s[j];
         }
@@ -290,13 +321,13 @@ static int attend_core(const uint16_t *q, const uint16_t *k_cache, const uint16_
             lse[r] = l;
             for (int64_t j = 0; j < nkeys; ++j) {
                 if (!visible[j]) continue;
-                const uint16_t *vrow;
-                if (j < ncache_cand)
-                    vrow = v_cache + coff[j];
-                else
-                    vrow = v_draft + (((int64_t)b * N + (j - ncache_cand)) * Hkv + hk) * d;
                 double p = exp(s[j] - l);
-                for (int c = 0; c < d; ++c) o[c] += p * bf16_to_double(vrow[c]);
+                if (j < ncache_cand) {
+                    for (int c = 0; c < d; ++c) o[c] += p * cache_value(cl, v_cache, vs, coff[j], c);
+                } else {
+                    const uint16_t *vrow = v_draft + (((int64_t)b * N + (j - ncache_cand)) * Hkv + hk) * d;
+                    for (int c = 0; c < d; ++c) o[c] += p * bf16_to_double(vrow[c]);
+                }
             }
         }
         free(visible);
@@ -313,7 +344,7 @@ int oracle_attend(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_
                   const int32_t *ctx_lens, float scale, int64_t cache_begin, int64_t cache_end,
                   const int64_t *rows, int64_t n_rows, double *out, double *lse)
 {
-    cache_layout cl = {stride_b, stride_h, stride_t, NULL, 0, 0, 0};
+    cache_layout cl = {stride_b, stride_h, stride_t, NULL, 0, 0, 0, 0, NULL, NULL};
     return attend_core(q, k_cache, v_cache, &cl, k_draft, v_draft, parent, idx, budget, B, N, Hq, Hkv, d,
                        L, ctx_lens, scale, cache_begin, cache_end, rows, n_rows, out, lse);
 }
@@ -330,10 +361,27 @@ int oracle_attend_paged(const uint16_t *q, const uint16_t *k_pool, const uint16_
 {
     if (!table || block_size < 1 || num_blocks < 0 || table_ld < (L + block_size - 1) / block_size)
         return ORACLE_INVALID_ARG;
-    cache_layout cl = {stride_blk, stride_h, stride_row, table, table_ld, block_size, num_blocks};
+    cache_layout cl = {stride_blk, stride_h, stride_row, table, table_ld, block_size, num_blocks, 0, NULL, NULL};
     return attend_core(q, k_pool, v_pool, &cl, k_draft, v_draft, parent, idx, budget, B, N, Hq, Hkv, d,
                        L, ctx_lens, scale, 0, L, rows, n_rows, out, lse);
 }
+
+/* The same attention over a cache of E4M3 codes (element strides, one byte an element) with
+   the K and V scales [B * Hkv] (value = code * scale); the queries and the draft block are bf16. */
+int oracle_attend_fp8(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                      int64_t stride_b, int64_t stride_h, int64_t stride_t, const float *k_scale,
+                      const float *v_scale, const uint16_t *k_draft, const uint16_t *v_draft,
+                      const int32_t *parent, const int32_t *idx, int budget, int B, int N, int Hq, int Hkv,
+                      int d, int L, const int32_t *ctx_lens, float scale, const int64_t *rows,
+                      int64_t n_rows, double *out, double *lse)
+{
+    cache_layout cl = {stride_b, stride_h, stride_t, NULL, 0, 0, 0, 1, k_scale, v_scale};
+    return attend_core(q, k_cache, v_cache, &cl, k_draft, v_draft, parent, idx, budget, B, N, Hq, Hkv, d,
+                       L, ctx_lens, scale, 0, L, rows, n_rows, out, lse);
+}
+
+/* E4M3 code -> double, for the tests that pin the decoding. */
+double oracle_e4m3_value(int code) { return e4m3_to_double((uint8_t)code); }
 
 /* ------------------------------------------------------------------------ */
 /* log-sum-exp merge of two normalised parts                                 */

@@ -38,7 +38,8 @@ MUTANTS = [
      "double wa = exp(la - l), wb = exp(la - l);"),
     ("one extra draft-tier token", "int m = top_m;", "int m = top_m + 1;"),
     ("tier 1 ranks by the target score", "pool[t - rest_lo].score = ds[t];", "pool[t - rest_lo].score = ts[t];"),
-    ("cache V read from K", "vrow = v_cache + coff[j];", "vrow = k_cache + coff[j];"),
+    ("cache V read from K", "o[c] += p * cache_value(cl, v_cache, vs, coff[j], c);",
+     "o[c] += p * cache_value(cl, k_cache, vs, coff[j], c);"),
     ("probability not normalised", "double p = exp(s[j] - l);", "double p = exp(s[j] - mx);"),
     ("sink one short", "for (int t = 0; t < s0; ++t) chosen[t] = 1;", "for (int t = 1; t < s0; ++t) chosen[t] = 1;"),
     ("paged: row inside the block", "(t % cl->block_size) * cl->st", "((t + 1) % cl->block_size) * cl->st"),
@@ -46,6 +47,11 @@ MUTANTS = [
      "cl->table[b * cl->table_ld + t / cl->block_size + 1]"),
     ("paged: block stride for the head stride", "*off = blk * cl->sb + hk * cl->sh", "*off = blk * cl->sh + hk * cl->sh"),
     ("paged: an entry one past the pool accepted", "blk >= cl->num_blocks", "blk > cl->num_blocks"),
+    ("fp8: subnormal exponent", "ldexp((double)m / 8.0, 1 - 7)", "ldexp((double)m / 8.0, 0 - 7)"),
+    ("fp8: exponent bias", "ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
+    ("fp8: sign dropped", "return sgn ? -v : v;", "return v;"),
+    ("fp8: the V scale on K", "cache_value(cl, k_cache, ks, coff[j], c)", "cache_value(cl, k_cache, vs, coff[j], c)"),
+    ("fp8: the next head's scale", "cl->k_scale + (int64_t)b * Hkv + hk", "cl->k_scale + (int64_t)b * Hkv + (hk + 1) % Hkv"),
 ]
 
 PIN_CALLS = [
@@ -65,6 +71,9 @@ PIN_CALLS = [
     lambda: pins.test_paged_equals_contiguous(4),
     lambda: pins.test_paged_bad_block_entry("pool_size"),
     pins.test_paged_entries_past_the_context_are_not_read,
+    pins.test_e4m3_decoding_table,
+    lambda: pins.test_fp8_equals_bf16_on_the_numbers_it_stands_for("dense"),
+    pins.test_fp8_v_scale_scales_the_cache_output_only,
 ]
 
 

@@ -494,3 +494,78 @@ def test_paged_entries_past_the_context_are_not_read():
     ro, rl, rs = oracle.attend(q, kc, vc, kd, vd, par, scale=0.3, ctx_lens=cl)
     assert ps == rs == 0
     assert np.array_equal(ro, po) and np.array_equal(rl, pl)
+
+
+# ---------------------------------------------------------------------------
+# fp8 cache (E4M3 codes, value = the code's number times a scale per sequence and KV head)
+
+
+def test_e4m3_decoding_table():
+    """Every code against torch's own float8_e4m3fn conversion (an independent implementation of
+    the OCP E4M3 format), and the format's landmarks by hand: subnormals m * 2^-9, bias 7, the
+    largest number 448, no infinities, S.1111.111 = NaN."""
+    ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64)
+    for c in range(256):
+        got, want = oracle.e4m3_value(c), float(ref[c])
+        assert (math.isnan(got) and math.isnan(want)) or got == want, (c, got, want)
+    hand = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0, 0x39: 1.125,
+            0x77: 240.0, 0x7E: 448.0, 0xFE: -448.0, 0xB8: -1.0}
+    for c, v in hand.items():
+        assert oracle.e4m3_value(c) == v, hex(c)
+    assert math.isnan(oracle.e4m3_value(0x7F)) and math.isnan(oracle.e4m3_value(0xFF))
+    assert math.copysign(1.0, oracle.e4m3_value(0x80)) == -1.0
+
+
+def fp8_codes(shape, gen):
+    """E4M3 codes with a random sign, exponent field 0..8 (subnormals included) and mantissa:
+    numbers of magnitude below 4, so that scores stay moderate."""
+    sign = torch.randint(0, 2, shape, generator=gen) << 7
+    exp_ = torch.randint(0, 9, shape, generator=gen) << 3
+    man = torch.randint(0, 8, shape, generator=gen)
+    return (sign | exp_ | man).to(torch.uint8)
+
+
+def fp8_problem(seed, B=2, N=5, Hq=8, Hkv=2, L=150, d=128):
+    """A bf16 problem (queries, draft block, tree) with an E4M3 cache and power-of-two scales per
+    (sequence, KV head); also the bf16 cache holding exactly the numbers the codes stand for."""
+    g = torch.Generator().manual_seed(seed)
+    x = W.make_inputs(W.Workload("fp8", B=B, L=L, Hq=Hq, Hkv=Hkv, N=N, tree="random", depth_max=3, seed=seed))
+    kc, vc = fp8_codes((B, Hkv, L, d), g), fp8_codes((B, Hkv, L, d), g)
+    ks = 2.0 ** torch.randint(-3, 3, (B, Hkv), generator=g).to(torch.float32)
+    vs = 2.0 ** torch.randint(-3, 3, (B, Hkv), generator=g).to(torch.float32)
+
+    def values(codes, sc):  # exact: a 4-bit mantissa times a power of two fits bf16
+        v = codes.view(torch.float8_e4m3fn).to(torch.float32) * sc[:, :, None, None]
+        return v.to(torch.bfloat16)
+
+    return x, kc, vc, ks, vs, values(kc, ks), values(vc, vs)
+
+
+@pytest.mark.parametrize("mode", ["dense", "sparse", "ragged"])
+def test_fp8_equals_bf16_on_the_numbers_it_stands_for(mode):
+    x, kc, vc, ks, vs, kb, vb = fp8_problem(11 if mode == "dense" else 12)
+    B, L = kc.shape[0], kc.shape[2]
+    kw = {}
+    if mode == "sparse":
+        ds, ts = W.random_scores(B, L, seed=5)
+        idx = torch.from_numpy(oracle.select(ds, ts, sink=4, window=16, top_m=20, budget=64)[0])
+        kw["idx"] = idx
+    if mode == "ragged":
+        kw["ctx_lens"] = torch.tensor([L, 37], dtype=torch.int32)
+    o8, l8, s8 = oracle.attend_fp8(x["q"], kc, vc, ks, vs, x["k_draft"], x["v_draft"], x["parent"],
+                                   scale=x["scale"], **kw)
+    ob, lb, sb = oracle.attend(x["q"], kb, vb, x["k_draft"], x["v_draft"], x["parent"], scale=x["scale"], **kw)
+    assert s8 == sb == 0
+    assert np.array_equal(o8, ob) and np.array_equal(l8, lb)
+
+
+def test_fp8_v_scale_scales_the_cache_output_only():
+    """No draft block: doubling every V scale doubles out exactly and leaves lse alone; doubling
+    every K scale while halving the softmax scale changes nothing."""
+    x, kc, vc, ks, vs, _, _ = fp8_problem(13)
+    args = (x["q"], kc, vc)
+    o1, l1, _ = oracle.attend_fp8(*args, ks, vs, None, None, None, scale=x["scale"])
+    o2, l2, _ = oracle.attend_fp8(*args, ks, 2 * vs, None, None, None, scale=x["scale"])
+    o3, l3, _ = oracle.attend_fp8(*args, 2 * ks, vs, None, None, None, scale=x["scale"] / 2)
+    assert np.array_equal(o2, 2 * o1) and np.array_equal(l2, l1)
+    assert np.array_equal(o3, o1) and np.array_equal(l3, l1)
