@@ -158,7 +158,8 @@ spec_status_t spec_verify_attn_sparse(const uint16_t *q, const uint16_t *k_cache
                                       void *workspace, size_t ws_bytes, void *stream);
 
 /* ------------------------------------------------------------------------ */
-/* Verification attention with extensions: a paged KV cache and a bf16 output.
+/* Verification attention with extensions: a paged KV cache, an fp8 KV cache and a
+ * bf16 output.
  *
  * The source pages use neither; they are layouts of serving engines. With
  * idx == NULL this is spec_verify_attn, with idx != NULL (`budget` entries
@@ -179,15 +180,28 @@ spec_status_t spec_verify_attn_sparse(const uint16_t *q, const uint16_t *k_cache
  * are multiples of 128 (others run on the warp-level kernel).
  * ext->out_dtype == SPEC_OUT_BF16: out is bf16 [B, N, Hq, d] (the fp32 result
  * rounded to nearest even); lse stays fp32.
+ * ext->kv_dtype == SPEC_KV_E4M3: k_cache and v_cache (contiguous or paged)
+ * hold E4M3 codes of the OCP 8-bit floating-point formats, one byte an
+ * element (pass the byte arrays through the uint16_t pointers; the strides
+ * count bytes and must be multiples of 16). The value of element (b, h, t, c)
+ * is the code's number times k_scale[b * Hkv + h] (v_scale for V): fp32
+ * device arrays [B * Hkv], 4-byte aligned. Queries and the draft block stay
+ * bf16. The fp8 cache runs on the warp-level tensor-core kernel, which
+ * converts the codes to bf16 in shared memory (exact) and folds the scales
+ * into the softmax scale and the partial's normalisation.
  * workspace: >= spec_verify_workspace_size(B, N, Hq, Hkv, d, idx ? budget : L).
  */
 typedef enum { SPEC_OUT_F32 = 0, SPEC_OUT_BF16 = 1 } spec_out_dtype_t;
+typedef enum { SPEC_KV_BF16 = 0, SPEC_KV_E4M3 = 1 } spec_kv_dtype_t;
 typedef struct {
     const int32_t *block_table; /* NULL: the contiguous cache of spec_verify_attn */
     int64_t table_ld;
     int block_size;
     int64_t num_blocks;
-    int out_dtype; /* spec_out_dtype_t */
+    int out_dtype;        /* spec_out_dtype_t */
+    int kv_dtype;         /* spec_kv_dtype_t */
+    const float *k_scale; /* E4M3 only: [B * Hkv] */
+    const float *v_scale;
 } spec_verify_ext;
 spec_status_t spec_verify_attn_ex(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                                   int64_t kv_stride_b, int64_t kv_stride_h, int64_t kv_stride_t,

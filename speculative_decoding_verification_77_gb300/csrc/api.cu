@@ -68,12 +68,16 @@ size_t verify_bytes_any(int B, int N, int Hq, int Hkv, int d, int L_eff, int sms
     return std::max(a, b) + align_up((size_t)B * L_eff * sizeof(int32_t), 256);
 }
 
-// Where a paged call's cache lives (all zero for a contiguous cache).
-struct PagedArgs {
+// The extended call's options: where a paged call's cache lives (all zero for a contiguous
+// cache), and an fp8 cache's scales.
+struct ExtArgs {
     const int32_t *table = nullptr;
     int64_t table_ld = 0;
     int block_size = 0;
     int64_t num_blocks = 0;
+    bool kv_fp8 = false;
+    const float *k_scale = nullptr;
+    const float *v_scale = nullptr;
 };
 
 spec_status_t verify_common(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
@@ -81,7 +85,7 @@ spec_status_t verify_common(const uint16_t *q, const uint16_t *k_cache, const ui
                             const uint16_t *v_draft, const int32_t *parent, int B, int N, int Hq,
                             int Hkv, int d, int L, const int32_t *ctx_lens, float scale,
                             const int32_t *idx, int budget, bool sparse, float *out, float *lse,
-                            void *workspace, size_t ws_bytes, void *stream, const PagedArgs &pg = PagedArgs(),
+                            void *workspace, size_t ws_bytes, void *stream, const ExtArgs &pg = ExtArgs(),
                             bool out_bf16 = false) {
     // host checks, before anything is enqueued
     if (!q || !out || !lse || !workspace) return SPEC_ERR_INVALID_ARG;
@@ -98,6 +102,11 @@ spec_status_t verify_common(const uint16_t *q, const uint16_t *k_cache, const ui
     if (!(scale == scale)) return SPEC_ERR_INVALID_ARG;
     if (d != kHeadDim) return SPEC_ERR_UNSUPPORTED;
     if ((int64_t)B * N * Hq > (int64_t)1 << 31) return SPEC_ERR_INVALID_ARG;
+    if (pg.kv_fp8) {  // E4M3 codes: one byte an element, rows copied 16 bytes at a time
+        if (L > 0 && (!pg.k_scale || !pg.v_scale || !aligned(pg.k_scale, 4) || !aligned(pg.v_scale, 4)))
+            return SPEC_ERR_INVALID_ARG;
+        if (sb % 16 || sh % 16 || st % 16) return SPEC_ERR_INVALID_ARG;
+    }
     if (pg.table) {  // paged cache
         if (pg.block_size < 1 || pg.num_blocks < 0 || st < 1 || !aligned(pg.table, 4) ||
             pg.table_ld < ((int64_t)L + pg.block_size - 1) / pg.block_size)
@@ -138,6 +147,9 @@ spec_status_t verify_common(const uint16_t *q, const uint16_t *k_cache, const ui
     a.num_blocks = pg.num_blocks;
     a.idx_resolved = 0;
     a.out_bf16 = out_bf16 ? 1 : 0;
+    a.kv_fp8 = pg.kv_fp8 ? 1 : 0;
+    a.k_scale = pg.k_scale;
+    a.v_scale = pg.v_scale;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (const cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s); e != cudaSuccess) return (spec_status_t)cuda_failure(e);
@@ -271,15 +283,19 @@ spec_status_t spec_verify_attn_ex(const uint16_t *q, const uint16_t *k_cache, co
                                   int N, int Hq, int Hkv, int d, int L, const int32_t *ctx_lens, float scale,
                                   const int32_t *idx, int budget, const spec_verify_ext *ext, void *out, float *lse,
                                   void *workspace, size_t ws_bytes, void *stream) {
-    PagedArgs pg;
+    ExtArgs pg;
     bool bf16 = false;
     if (ext) {
         if (ext->out_dtype != SPEC_OUT_F32 && ext->out_dtype != SPEC_OUT_BF16) return SPEC_ERR_INVALID_ARG;
+        if (ext->kv_dtype != SPEC_KV_BF16 && ext->kv_dtype != SPEC_KV_E4M3) return SPEC_ERR_INVALID_ARG;
         bf16 = ext->out_dtype == SPEC_OUT_BF16;
         pg.table = ext->block_table;
         pg.table_ld = ext->table_ld;
         pg.block_size = ext->block_size;
         pg.num_blocks = ext->num_blocks;
+        pg.kv_fp8 = ext->kv_dtype == SPEC_KV_E4M3;
+        pg.k_scale = ext->k_scale;
+        pg.v_scale = ext->v_scale;
     }
     return verify_common(q, k_cache, v_cache, kv_stride_b, kv_stride_h, kv_stride_t, k_draft, v_draft, parent, B, N,
                          Hq, Hkv, d, L, ctx_lens, scale, idx, budget, idx != nullptr, static_cast<float *>(out), lse,

@@ -16,6 +16,15 @@
 // Layout: 4 warps, each owning 16 query rows; 64-token K/V tiles double
 // buffered in shared memory by cp.async (16-byte, XOR-swizzled rows); S = QK^T
 // and O += PV with mma.m16n8k16 bf16 -> fp32; online softmax in base 2.
+//
+// fp8 cache (FP8): the rows are E4M3 codes, 128 bytes each, double buffered by
+// cp.async in a staging area; before a tile is used, the CTA converts its codes
+// into the bf16 tile layout above (every E4M3 number is exact in bf16), and the
+// per-(sequence, KV head) scales enter as a factor of the softmax scale (K) and
+// of the partial's normalisation (V), so the MMAs stay bf16.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 
 namespace specverify {
@@ -29,6 +38,10 @@ constexpr int STAGES = 2;
 constexpr int THREADS = 128;
 constexpr int TILE_BYTES = BN * D * 2;  // 16 KiB
 constexpr int SMEM_BYTES = BM * D * 2 + STAGES * 2 * TILE_BYTES + STAGES * BN;
+// fp8: the first stage's K|V area holds the converted bf16 tile, the second the staged codes
+constexpr int ROW8_BYTES = D;                 // 128 codes
+constexpr int TILE8_BYTES = BN * ROW8_BYTES;  // 8 KiB
+static_assert(STAGES * 2 * TILE8_BYTES <= 2 * TILE_BYTES, "staged codes fit one stage's area");
 
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {  // byte offset in a [rows][128] bf16 tile
     return (uint32_t)(row * 256 + ((chunk ^ (row & 7)) << 4));
@@ -68,6 +81,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Two E4M3 codes (the lower byte first) -> the bf16 pair of the same numbers (exact:
+// E4M3 -> f16 is exact, and so is f16 -> f32 -> bf16 for every E4M3 number).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+    return pack_bf16(f.x, f.y);
+}
+
 // Token held by cache position p of sequence b, or -1 when the position is
 // masked. Sparse: p indexes idx[b]; an entry is used iff it is in [0, n) and
 // above the previous entry; anything but -1 padding that is unused is flagged.
@@ -77,13 +98,14 @@ __device__ __forceinline__ int cache_token(const VerifyArgs &a, int b, int n, in
     return sparse_token(a, b, n, p, report);
 }
 
-template <bool SPARSE>
+template <bool SPARSE, bool FP8>
 __global__ void __launch_bounds__(THREADS, 2) cache_attn_mma_kernel(VerifyArgs a, SplitPlan p) {
     griddep_launch_dependents();  // the merge may be scheduled as this grid's CTAs drain
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *sQ = smem;
     uint8_t *sKV = smem + BM * D * 2;  // [stage][K|V][BN][D]
     uint8_t *sValid = sKV + STAGES * 2 * TILE_BYTES;
+    uint8_t *sCodes = sKV + 2 * TILE_BYTES;  // fp8: [stage][K|V][BN][128 codes]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gq = lane >> 2, tq = lane & 3;
@@ -99,6 +121,9 @@ __global__ void __launch_bounds__(THREADS, 2) cache_attn_mma_kernel(VerifyArgs a
         const int hk = (int)((u / p.row_groups) % a.Hkv);
         const int b = (int)(u / ((int64_t)p.row_groups * a.Hkv));
         const int n = context_len(a, b);
+        // fp8: the K scale joins the softmax scale, the V scale the partial's normalisation
+        const float sl2u = FP8 ? sl2 * __ldg(a.k_scale + (int64_t)b * a.Hkv + hk) : sl2;
+        const float vscale = FP8 ? __ldg(a.v_scale + (int64_t)b * a.Hkv + hk) : 1.f;
 
         // Q rows of this unit -> shared memory (zero rows past G*N)
         __syncthreads();
@@ -113,6 +138,24 @@ __global__ void __launch_bounds__(THREADS, 2) cache_attn_mma_kernel(VerifyArgs a
         cp_async_commit();
 
         auto load_tile = [&](int tile, int stage) {
+            if (FP8) {  // 8 chunks of 16 codes a row, unswizzled in the staging area
+                uint8_t *sK8 = sCodes + (stage * 2) * TILE8_BYTES;
+                uint8_t *sV8 = sK8 + TILE8_BYTES;
+                const uint8_t *k8 = reinterpret_cast<const uint8_t *>(a.k_cache);
+                const uint8_t *v8 = reinterpret_cast<const uint8_t *>(a.v_cache);
+                for (int c = tid; c < BN * 8; c += THREADS) {
+                    const int row = c >> 3, ch = c & 7;
+                    const int t = cache_token<SPARSE>(a, b, n, tile * BN + row, ch == 0);
+                    const int64_t roff = t >= 0 ? cache_row_offset(a, b, hk, t, ch == 0) : -1;
+                    const bool ok = roff >= 0;
+                    const int64_t off = roff + ch * 16;  // one byte an element
+                    cp_async16(smem_addr(sK8 + row * ROW8_BYTES + ch * 16), ok ? (const void *)(k8 + off) : (const void *)a.q, ok);
+                    cp_async16(smem_addr(sV8 + row * ROW8_BYTES + ch * 16), ok ? (const void *)(v8 + off) : (const void *)a.q, ok);
+                    if (ch == 0) sValid[stage * BN + row] = ok;
+                }
+                cp_async_commit();
+                return;
+            }
             uint8_t *sK = sKV + (stage * 2) * TILE_BYTES;
             uint8_t *sV = sK + TILE_BYTES;
             for (int c = tid; c < BN * 16; c += THREADS) {
@@ -152,9 +195,26 @@ __global__ void __launch_bounds__(THREADS, 2) cache_attn_mma_kernel(VerifyArgs a
                 }
             }
             const int stage = it % STAGES;
-            const uint8_t *sK = sKV + (stage * 2) * TILE_BYTES;
+            const uint8_t *sK = sKV + (FP8 ? 0 : stage * 2) * TILE_BYTES;
             const uint8_t *sV = sK + TILE_BYTES;
             const uint8_t *valid = sValid + stage * BN;
+            if (FP8) {  // the staged codes -> the bf16 tile (16 codes = two 16-byte bf16 chunks)
+                const uint8_t *sK8 = sCodes + (stage * 2) * TILE8_BYTES;
+                for (int c = tid; c < 2 * BN * 8; c += THREADS) {
+                    const int kv = c >= BN * 8, cc = c - kv * BN * 8;
+                    const int row = cc >> 3, ch = cc & 7;
+                    const uint4 codes = *reinterpret_cast<const uint4 *>(sK8 + kv * TILE8_BYTES + row * ROW8_BYTES + ch * 16);
+                    uint8_t *dst = sKV + kv * TILE_BYTES;
+                    uint4 lo, hi;
+                    lo.x = e4m3x2_to_bf16x2(codes.x & 0xffffu); lo.y = e4m3x2_to_bf16x2(codes.x >> 16);
+                    lo.z = e4m3x2_to_bf16x2(codes.y & 0xffffu); lo.w = e4m3x2_to_bf16x2(codes.y >> 16);
+                    hi.x = e4m3x2_to_bf16x2(codes.z & 0xffffu); hi.y = e4m3x2_to_bf16x2(codes.z >> 16);
+                    hi.z = e4m3x2_to_bf16x2(codes.w & 0xffffu); hi.w = e4m3x2_to_bf16x2(codes.w >> 16);
+                    *reinterpret_cast<uint4 *>(dst + swz(row, 2 * ch)) = lo;
+                    *reinterpret_cast<uint4 *>(dst + swz(row, 2 * ch + 1)) = hi;
+                }
+                __syncthreads();
+            }
 
             // S = Q K^T for this warp's 16 rows x 64 tokens
             float s[8][4];
@@ -178,10 +238,10 @@ __global__ void __launch_bounds__(THREADS, 2) cache_attn_mma_kernel(VerifyArgs a
             for (int nt = 0; nt < 8; ++nt) {
                 const int j = nt * 8 + tq * 2;
                 const bool v0 = valid[j], v1 = valid[j + 1];
-                s[nt][0] = v0 ? s[nt][0] * sl2 : -INFINITY;
-                s[nt][1] = v1 ? s[nt][1] * sl2 : -INFINITY;
-                s[nt][2] = v0 ? s[nt][2] * sl2 : -INFINITY;
-                s[nt][3] = v1 ? s[nt][3] * sl2 : -INFINITY;
+                s[nt][0] = v0 ? s[nt][0] * sl2u : -INFINITY;
+                s[nt][1] = v1 ? s[nt][1] * sl2u : -INFINITY;
+                s[nt][2] = v0 ? s[nt][2] * sl2u : -INFINITY;
+                s[nt][3] = v1 ? s[nt][3] * sl2u : -INFINITY;
                 mx[0] = fmaxf(mx[0], fmaxf(s[nt][0], s[nt][1]));
                 mx[1] = fmaxf(mx[1], fmaxf(s[nt][2], s[nt][3]));
             }
@@ -238,7 +298,7 @@ __global__ void __launch_bounds__(THREADS, 2) cache_attn_mma_kernel(VerifyArgs a
             l += __shfl_xor_sync(0xffffffffu, l, 2);
             const int row = warp * 16 + gq + r * 8;
             if (rg * BM + row >= M) continue;
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float inv = l > 0.f ? vscale / l : 0.f;
             float *dst = a.o_part + (slot * BM + row) * D;
 #pragma unroll
             for (int nt = 0; nt < 16; ++nt)
@@ -257,11 +317,15 @@ int mma_tile_tokens() { return BN; }
 
 cudaError_t launch_cache_attn_mma(const VerifyArgs &a, const SplitPlan &p, bool sparse,
                                   cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1) {
-    auto kern = sparse ? cache_attn_mma_kernel<true> : cache_attn_mma_kernel<false>;
+    auto kern = a.kv_fp8 ? (sparse ? cache_attn_mma_kernel<true, true> : cache_attn_mma_kernel<false, true>)
+                         : (sparse ? cache_attn_mma_kernel<true, false> : cache_attn_mma_kernel<false, false>);
     static PerDeviceOnce attr_once;
     cudaError_t e = once_per_device(attr_once, [] {
-        const cudaError_t r = kernel_attributes(cache_attn_mma_kernel<false>, SMEM_BYTES);
-        return r != cudaSuccess ? r : kernel_attributes(cache_attn_mma_kernel<true>, SMEM_BYTES);
+        cudaError_t r = cudaSuccess;
+        for (auto k : {cache_attn_mma_kernel<false, false>, cache_attn_mma_kernel<true, false>,
+                       cache_attn_mma_kernel<false, true>, cache_attn_mma_kernel<true, true>})
+            if (r == cudaSuccess) r = kernel_attributes(k, SMEM_BYTES);
+        return r;
     });
     if (e != cudaSuccess) return e;
     if (ev0) cudaEventRecord(ev0, s);

@@ -437,6 +437,7 @@ bool encode_map(CUtensorMap *map, const void *base, int rank, const cuuint64_t *
 }  // namespace
 
 bool tc_supported(const VerifyArgs &a) {
+    if (a.kv_fp8) return false;  // the tensor-core tiles are bf16
     // the softmax takes the row max of the raw scores, which needs scale > 0
     if (!(a.G >= 1 && a.G <= 128 && (128 % a.G) == 0 && a.scale > 0.f)) return false;
     if (a.idx)  // gathered rows are copied 16 bytes at a time: every row start 16-byte aligned

@@ -220,6 +220,11 @@ struct VerifyArgs {
     int64_t num_blocks;
     int idx_resolved;  // sparse: idx holds validated pool rows (entry >= 0: used), see paged.cu
     int out_bf16;      // out is bf16 [B, N, Hq, d] (rounded to nearest even) instead of fp32
+    // fp8 cache: k_cache / v_cache hold E4M3 codes (one byte an element, element strides);
+    // the value is the code's number times k_scale / v_scale [b * Hkv + h] (fp32)
+    int kv_fp8;
+    const float *k_scale;
+    const float *v_scale;
 };
 
 // Context length of sequence b, clamped to [0, L]; out-of-range values flag bad input.

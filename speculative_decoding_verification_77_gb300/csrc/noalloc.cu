@@ -120,6 +120,9 @@ extern "C" spec_status_t spec_verify_attn_noalloc(
     a.num_blocks = 0;
     a.idx_resolved = 0;
     a.out_bf16 = 0;
+    a.kv_fp8 = 0;
+    a.k_scale = nullptr;
+    a.v_scale = nullptr;
     a.o_part = reinterpret_cast<float *>(ws + kHeaderBytes);
     a.lse_part = reinterpret_cast<float *>(ws + kHeaderBytes +
                                            align_up((size_t)plan.slots * plan.BM * d * sizeof(float), 256));

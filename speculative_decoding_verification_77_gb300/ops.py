@@ -213,13 +213,18 @@ def verify_attn_sparse(q, k_cache, v_cache, k_draft, v_draft, parent, idx, *, sc
 
 class _VerifyExt(ctypes.Structure):
     _fields_ = [("block_table", ctypes.c_void_p), ("table_ld", ctypes.c_int64), ("block_size", ctypes.c_int),
-                ("num_blocks", ctypes.c_int64), ("out_dtype", ctypes.c_int)]
+                ("num_blocks", ctypes.c_int64), ("out_dtype", ctypes.c_int), ("kv_dtype", ctypes.c_int),
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p)]
 
 
 def verify_attn_ex(q, k_cache, v_cache, k_draft=None, v_draft=None, parent=None, *, L: int | None = None, idx=None,
-                   block_table=None, out_dtype=torch.float32, scale=None, ctx_lens=None, out=None, lse=None, ws=None):
-    """Verification attention with the extensions of spec_verify_attn_ex: a paged cache and/or a
-    bf16 output (dense, or sparse with idx [B, budget]).
+                   block_table=None, out_dtype=torch.float32, scale=None, ctx_lens=None, out=None, lse=None, ws=None,
+                   k_scale=None, v_scale=None):
+    """Verification attention with the extensions of spec_verify_attn_ex: a paged cache, an fp8
+    cache and/or a bf16 output (dense, or sparse with idx [B, budget]).
+
+    fp8 cache: k_cache/v_cache torch.float8_e4m3fn (or uint8 codes) with k_scale, v_scale fp32
+    [B, Hkv] (the value of a code is its E4M3 number times the scale of its sequence and head).
 
     Contiguous: k_cache/v_cache [B, Hkv, L, d]. Paged (block_table int32 [B, max_blocks]):
     k_cache/v_cache are the pools, [num_blocks, Hkv, block_size, d] bf16 views (any strides, d
@@ -229,8 +234,18 @@ def verify_attn_ex(q, k_cache, v_cache, k_draft=None, v_draft=None, parent=None,
     Returns (out [B,N,Hq,d] of out_dtype, lse fp32 [B,N,Hq]).
     """
     lib = load_library()
-    for t, nm in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (k_draft, "k_draft"), (v_draft, "v_draft")):
+    fp8 = k_cache.dtype in (torch.float8_e4m3fn, torch.uint8)
+    for t, nm in ((q, "q"), (k_draft, "k_draft"), (v_draft, "v_draft")):
         _need(t, torch.bfloat16, nm, 4)
+    for t, nm in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, k_cache.dtype if fp8 else torch.bfloat16, nm, 4)
+    if fp8:
+        if k_scale is None or v_scale is None:
+            raise ValueError("an fp8 cache needs k_scale and v_scale [B, Hkv]")
+        _need(k_scale, torch.float32, "k_scale", 2)
+        _need(v_scale, torch.float32, "v_scale", 2)
+        if not (k_scale.is_contiguous() and v_scale.is_contiguous()):
+            raise ValueError("k_scale and v_scale must be contiguous [B, Hkv]")
     _need(block_table, torch.int32, "block_table", 2)
     _need(parent, torch.int32, "parent", 2)
     _need(ctx_lens, torch.int32, "ctx_lens", 1)
@@ -268,7 +283,8 @@ def verify_attn_ex(q, k_cache, v_cache, k_draft=None, v_draft=None, parent=None,
         ws = workspace(nbytes, dev, "verify")
     ext = _VerifyExt(None if block_table is None else block_table.data_ptr(),
                      0 if block_table is None else block_table.stride(0), bs, nblk,
-                     1 if out_dtype == torch.bfloat16 else 0)
+                     1 if out_dtype == torch.bfloat16 else 0, 1 if fp8 else 0,
+                     k_scale.data_ptr() if fp8 else None, v_scale.data_ptr() if fp8 else None)
     code = lib.spec_verify_attn_ex(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.stride(0), k_cache.stride(1), k_cache.stride(2), _ptr(k_draft),
         _ptr(v_draft), _ptr(parent), B, N, Hq, Hkv, d, L, _ptr(ctx_lens), ctypes.c_float(scale), _ptr(idx),

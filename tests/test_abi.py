@@ -154,6 +154,27 @@ def test_paged_rejects_bad_arguments_on_the_host(lib, over, code):
     assert lib.spec_verify_attn_ex(*a.values()) == code
 
 
+@pytest.mark.parametrize("over,code", [
+    (dict(kvd=7), 1), (dict(ks=None), 1), (dict(vs=None), 1), (dict(ks=18), 1),
+    # fp8 rows are copied 16 bytes at a time: strides (bytes) must be multiples of 16
+    (dict(st=136), 1), (dict(sh=1000), 1),
+])
+def test_fp8_rejects_bad_arguments_on_the_host(lib, over, code):
+    # fake, never-dereferenced addresses: every one of these checks returns before any CUDA call
+    from speculative_decoding_verification_77_gb300 import ops
+
+    e = dict(kvd=1, ks=16, vs=16)
+    for k in e:
+        if k in over:
+            e[k] = over.pop(k)
+    ext = ops._VerifyExt(None, 0, 0, 0, 0, e["kvd"], e["ks"], e["vs"])
+    a = dict(q=16, kc=16, vc=16, sb=300 * 128, sh=300 * 128, st=128, kd=None, vd=None, par=None, B=1, N=1, Hq=1,
+             Hkv=1, d=128, L=300, ctx=None, scale=ctypes.c_float(0.1), idx=None, budget=0, ext=ctypes.byref(ext),
+             out=16, lse=16, ws=256, ws_bytes=1 << 30, stream=None)
+    a.update(over)
+    assert lib.spec_verify_attn_ex(*a.values()) == code
+
+
 def test_merge_rejects_bad_arguments_on_the_host(lib):
     assert lib.spec_lse_merge(None, 4, 4, 4, 4, 4, 10, 128, None) == 1
     assert lib.spec_lse_merge(4, 4, 4, 4, 4, 4, -1, 128, None) == 1

@@ -704,6 +704,84 @@ def test_bf16_output_is_the_rounded_fp32_output(ops, case):
     assert np.abs(o - ro).max() <= ATOL_O + np.abs(ro).max() * 2.0 ** -8
 
 
+# ---------------------------------------------------------------- fp8 KV cache
+
+
+def quantize_e4m3(c):
+    """A bf16 cache [B, Hkv, L, d] as E4M3 codes with one fp32 scale per (sequence, KV head): the
+    head's largest magnitude maps to 448, the format's largest number."""
+    amax = c.float().abs().amax(dim=(2, 3)).clamp_min(1e-30)
+    sc = (amax / 448.0).to(torch.float32)
+    return (c.float() / sc[:, :, None, None]).to(torch.float8_e4m3fn), sc
+
+
+def codes_to_pool(kc, vc, bs, gen):
+    """The code caches scattered into a pool of bs-row blocks in a random order, noise blocks
+    between them: (k_pool, v_pool [nblk, Hkv, bs, d] codes, table [B, nb + 2], nblk)."""
+    B, Hkv, L, d = kc.shape
+    nb = (L + bs - 1) // bs
+    total = B * nb + 3
+    perm = torch.randperm(total, generator=gen)
+    noise = lambda: torch.randint(0, 120, (total, Hkv, bs, d), generator=gen).to(torch.uint8)
+    kp, vp = noise(), noise()
+    table = torch.full((B, nb + 2), -7, dtype=torch.int32)
+    for b in range(B):
+        for j in range(nb):
+            blk = int(perm[b * nb + j])
+            table[b, j] = blk
+            t0, t1 = j * bs, min(L, (j + 1) * bs)
+            kp[blk, :, : t1 - t0] = kc[b, :, t0:t1].view(torch.uint8)
+            vp[blk, :, : t1 - t0] = vc[b, :, t0:t1].view(torch.uint8)
+    return kp, vp, table, total
+
+
+@pytest.mark.parametrize("case", ["dense", "sparse", "paged_bs16", "sparse_paged_bs64", "g3", "ragged",
+                                  "bf16_out", "headline_sampled"])
+def test_fp8_cache_matches_oracle(ops, case):
+    """An E4M3 cache with a scale per (sequence, KV head) against the fp8 oracle on the same codes
+    and scales (the oracle is pinned to the bf16 one on the numbers the codes stand for)."""
+    if case == "headline_sampled":
+        w = W.workload(2)
+        x = W.make_inputs(w)
+        B, N, Hq, L = w.B, w.N, w.Hq, w.L
+    else:
+        Hq, Hkv = (12, 4) if case == "g3" else (8, 2)
+        B, N, L = 2, 6, 1000
+        x = small(300 + len(case), B=B, N=N, Hq=Hq, Hkv=Hkv, L=L)
+    kc, ks = quantize_e4m3(x["k_cache"])
+    vc, vs = quantize_e4m3(x["v_cache"])
+    g = to_dev(x)
+    kw, okw = {}, {}
+    rows = sample_rows(B, N, Hq, 384, seed=7) if case == "headline_sampled" else None
+    if "sparse" in case:
+        ds, ts = W.random_scores(B, L, seed=11)
+        idx, _, _ = oracle.select(ds, ts, sink=4, window=16, top_m=64, budget=256)
+        kw["idx"] = torch.from_numpy(idx).to(dev())
+        okw["idx"] = torch.from_numpy(idx)
+    if case == "ragged":
+        cl = torch.tensor([L, 357], dtype=torch.int32)
+        kw["ctx_lens"] = cl.to(dev())
+        okw["ctx_lens"] = cl
+    dk, dv = kc.to(dev()), vc.to(dev())
+    if "paged" in case:
+        bs = int(case.split("_bs")[1])
+        kp, vp, table, nblk = codes_to_pool(kc, vc, bs, torch.Generator().manual_seed(bs))
+        dk, dv = kp[:nblk].to(dev()), vp[:nblk].to(dev())
+        kw.update(block_table=table.to(dev()), L=L)
+    out_dtype = torch.bfloat16 if case == "bf16_out" else torch.float32
+    out, lse = ops.verify_attn_ex(g["q"], dk, dv, g["k_draft"], g["v_draft"], g["parent"], scale=x["scale"],
+                                  k_scale=ks.to(dev()), v_scale=vs.to(dev()), out_dtype=out_dtype, **kw)
+    ro, rl, st = oracle.attend_fp8(x["q"], kc, vc, ks, vs, x["k_draft"], x["v_draft"], x["parent"],
+                                   scale=x["scale"], rows=rows, **okw)
+    assert st == 0
+    torch.cuda.synchronize()
+    if case == "bf16_out":
+        o = out.float().cpu().numpy().reshape(ro.shape)
+        assert np.abs(o - ro).max() <= ATOL_O + np.abs(ro).max() * 2.0 ** -8
+    else:
+        assert_attn_close(out, lse, ro, rl, rows)
+
+
 def test_importance_scores_headline_shape(ops):
     """The headline layer (B=4, L=32k, N=64 tree) scored on two heads of different KV heads,
     against the oracle on a sample of tokens of every sequence (all draft queries of each)."""
