@@ -255,6 +255,29 @@ def test_needle_positions(ops, pos):
     assert_attn_close(out, lse, ro, rl, rows)
 
 
+@pytest.mark.parametrize("needles", [((138, 50.0), (198, 100.0)), ((200, 50.0), (9000, 120.0)),
+                                     ((70, 60.0), (4100, 130.0), (8190, 200.0))])
+def test_huge_logit_jumps_rescale_o(ops, needles):
+    """Keys whose logits jump far above everything before them (by more than 64 in base 2,
+    about 44 natural) later in the cache, also in consecutive halves of one tile: O must be
+    rescaled while earlier PV products may still be running."""
+    x = small(77, B=1, N=2, Hq=4, Hkv=2, L=10000)
+    q, scale = x["q"], x["scale"]
+    qv = q[0, 0, 2].double()
+    for pos, logit in needles:
+        x["k_cache"][0, 1, pos] = (qv * (logit / (scale * float(qv.dot(qv))))).to(torch.bfloat16)
+    g = to_dev(x)
+    out, lse = ops.verify_attn(g["q"], g["k_cache"], g["v_cache"], g["k_draft"], g["v_draft"], g["parent"],
+                               scale=scale)
+    ro, rl, _ = oracle.attend(x["q"], x["k_cache"], x["v_cache"], x["k_draft"], x["v_draft"], x["parent"],
+                              scale=scale)
+    torch.cuda.synchronize()
+    strongest = max(needles, key=lambda n: n[1])[0]
+    o = out.cpu().numpy().reshape(-1, 128)[2]
+    assert np.abs(o - x["v_cache"][0, 1, strongest].float().numpy()).max() < 2e-2
+    assert_attn_close(out, lse, ro, rl)
+
+
 def test_strided_cache_layout(ops):
     """K/V as [B, L, Hkv, d] memory viewed as [B, Hkv, L, d] (token-major cache)."""
     x = small(8, B=2, L=400, Hq=8, Hkv=4)
