@@ -471,6 +471,51 @@ def time_lse_merge(dev, stream, args, peaks, peak_src, windows):
     return e
 
 
+def time_fp8(dev, stream, args, peaks, peak_src, windows):
+    """The headline layer (B=4, L=32k, N=64 tree) over an fp8 cache: the bf16 cache quantised to
+    E4M3 codes with a scale per (sequence, KV head), verified through spec_verify_attn_ex (the
+    warp-level tensor-core kernel converts the codes to bf16 in shared memory). Algorithmic bytes:
+    the codes, 1 B an element (268 MB)."""
+    from speculative_decoding_verification_77_gb300 import ops
+
+    w = W.workload(2)
+    case = Case(w, dev)
+
+    def quantize(c):
+        amax = c.float().abs().amax(dim=(2, 3)).clamp_min(1e-30)
+        sc = (amax / 448.0).to(torch.float32)
+        return (c.float() / sc[:, :, None, None]).to(torch.float8_e4m3fn), sc
+
+    kc, ks = quantize(case.g["k_cache"])
+    vc, vs = quantize(case.g["v_cache"])
+    for k in ("k_cache", "v_cache"):  # the bf16 caches are no longer needed
+        del case.g[k]
+    torch.cuda.empty_cache()
+    g = case.g
+
+    def run(t):
+        ops.verify_attn_ex(t["q"], kc, vc, t["k_draft"], t["v_draft"], t["parent"], scale=case.scale, k_scale=ks,
+                           v_scale=vs, out=case.out, lse=case.lse)
+
+    for _ in range(3):
+        run(g)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    v = time_loop(case, run, stream, args.steps, args.extra_seconds / 2)
+    t1 = time.time()
+    ms = sum(v) / len(v)
+    nbytes = kc.numel() + vc.numel()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    e = {"workload": w.name + " over an E4M3 cache (scale per sequence and KV head)", "us_per_step": round(ms * 1e3, 2),
+         "kv_bytes_per_step": nbytes, "achieved_gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
+         "kernel": "cache_attn_mma<fp8> (mma.sync; codes converted to bf16 tiles in shared memory) + merge",
+         "l2": "inputs larger than L2, no flush", "peaks": f"{peak_src}: hbm {peaks['hbm_gbs']} GB/s",
+         "steps_timed": len(v)}
+    windows.append((e, t0, t1))
+    case.release()
+    return e
+
+
 def bastion_calibration(sweep, marginals, peaks, args):
     """BASTION's budget controller calibrated on the measured tree-size sweep: T_verify(N) =
     a T_roof(N) + c fitted to the sweep's step times, then the best-first growth and the
@@ -551,7 +596,7 @@ def run_native(args, ws_, rank, local):
     bastion = None
     windows = []
     if ws_ == 1 and args.extras != "none":
-        tokens = args.extras.split(",") if args.extras != "all" else ["1", "2", "3", "4", "5", "merge"]
+        tokens = args.extras.split(",") if args.extras != "all" else ["1", "2", "3", "4", "5", "merge", "fp8"]
         wanted = [int(c) for c in tokens if c.isdigit()]
         sweep = []
         marginals = None
@@ -575,6 +620,8 @@ def run_native(args, ws_, rank, local):
             extras["importance-scores-llama3-8b-layer"] = time_importance(dev, stream, args, peaks, peak_src, windows)
         if "merge" in tokens:
             extras["lse-merge2-131072-rows"] = time_lse_merge(dev, stream, args, peaks, peak_src, windows)
+        if "fp8" in tokens:
+            extras["fp8-cache-llama3-8b-layer"] = time_fp8(dev, stream, args, peaks, peak_src, windows)
         if sweep and marginals is not None:
             head_e = None
             if w.tree == "best_first" and w.name.startswith("tree-sweep"):
