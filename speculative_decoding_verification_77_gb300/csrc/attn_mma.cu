@@ -22,9 +22,6 @@
 // into the bf16 tile layout above (every E4M3 number is exact in bf16), and the
 // per-(sequence, KV head) scales enter as a factor of the softmax scale (K) and
 // of the partial's normalisation (V), so the MMAs stay bf16.
-#include <cuda_fp16.h>
-#include <cuda_fp8.h>
-
 #include "common.cuh"
 
 namespace specverify {
@@ -81,13 +78,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// Two E4M3 codes (the lower byte first) -> the bf16 pair of the same numbers (exact:
-// E4M3 -> f16 is exact, and so is f16 -> f32 -> bf16 for every E4M3 number).
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
-    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
-    return pack_bf16(f.x, f.y);
-}
 
 // Token held by cache position p of sequence b, or -1 when the position is
 // masked. Sparse: p indexes idx[b]; an entry is used iff it is in [0, n) and

@@ -81,7 +81,7 @@ __device__ __forceinline__ void load_q(const CUtensorMap *tm_q, uint8_t *sQ, uin
     }
 }
 
-template <bool SPARSE, bool PAGED>
+template <bool SPARSE, bool PAGED, bool FP8>
 __global__ void __launch_bounds__(THREADS, 1)
 cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
                      const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -92,6 +92,9 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint8_t *sQ = smem;
     uint8_t *sRing = smem + SMEM_RING;
+    // fp8 cache: a ring of RING - 1 bf16 tiles, then the staging of two items of codes
+    constexpr int KRING = FP8 ? RING - 1 : RING;
+    uint8_t *sStage = sRing + KRING * SLOT_BYTES;
     Bars &bs = *reinterpret_cast<Bars *>(smem + SMEM_BAR);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -113,6 +116,8 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
             mbar_init(&bs.o_done[h], 1);
             mbar_init(&bs.o_empty[h], 4);
         }
+        mbar_init(&bs.st_full[0], 1);
+        mbar_init(&bs.st_full[1], 1);
         mbar_init(&bs.mma_done, 1);
         bs.abort = 0;
         fence_mbar_init();
@@ -137,7 +142,10 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
         __syncwarp();
     } else if (warp == WARP_PRODUCER) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0) produce_dense<PAGED>(bs, sRing, &tm_q, &tm_k, &tm_v, a, p, split_tiles, u_first, g0, g1, qload);
+        if (FP8)
+            produce_dense_fp8(bs, sRing, sStage, &tm_q, &tm_k, &tm_v, a, p, split_tiles, u_first, g0, g1, lane, qload);
+        else if (lane == 0)
+            produce_dense<PAGED>(bs, sRing, &tm_q, &tm_k, &tm_v, a, p, split_tiles, u_first, g0, g1, qload);
         __syncwarp();
     } else if (warp == WARP_MMA) {
         // ------------------------------------------------------------ MMA issuer
@@ -169,11 +177,11 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
                 int qk_done = 0;
                 auto issue_qk = [&](int h, int i) -> bool {
                     const uint32_t n = item_base + 2u * (uint32_t)(seg_tile(s, split_tiles, h, i) - s.tb);
-                    const uint32_t slot = n % RING;
+                    const uint32_t slot = n % KRING;
                     // pipe 1 of a shared tile reuses the K tile pipe 0 already waited for
-                    if ((split_tiles || h == 0) && !__all_sync(0xffffffffu, wait_bar(bs, &bs.kv_full[slot], (n / RING) & 1u, a.status)))
+                    if ((split_tiles || h == 0) && !__all_sync(0xffffffffu, wait_bar(bs, &bs.kv_full[slot], (n / KRING) & 1u, a.status)))
                         return false;
-                    if (SPARSE) fence_proxy_async_smem();  // the slot was written by cp.async (generic proxy)
+                    if (SPARSE || FP8) fence_proxy_async_smem();  // the slot was written by the generic proxy
                     const uint64_t dq = h ? dq1 : dq0;
                     const uint64_t dk = dk0 + (uint64_t)slot * (SLOT_BYTES >> 4);
                     const uint32_t d_tmem = tmem + 128u * h;
@@ -192,10 +200,10 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
                         !__all_sync(0xffffffffu, wait_bar(bs, &bs.o_empty[h], (pipe_segs[h] - 1) & 1, a.status)))
                         return false;
                     const uint32_t n = item_base + 2u * (uint32_t)(seg_tile(s, split_tiles, h, i) - s.tb) + 1u;
-                    const uint32_t slot = n % RING;
-                    if ((split_tiles || h == 0) && !__all_sync(0xffffffffu, wait_bar(bs, &bs.kv_full[slot], (n / RING) & 1u, a.status)))
+                    const uint32_t slot = n % KRING;
+                    if ((split_tiles || h == 0) && !__all_sync(0xffffffffu, wait_bar(bs, &bs.kv_full[slot], (n / KRING) & 1u, a.status)))
                         return false;
-                    if (SPARSE) fence_proxy_async_smem();  // the slot was written by cp.async (generic proxy)
+                    if (SPARSE || FP8) fence_proxy_async_smem();  // the slot was written by the generic proxy
                     tc_fence_after();  // P_h was written to TMEM by the softmax warps
                     const uint64_t dv = dv0 + (uint64_t)slot * (SLOT_BYTES >> 4);
                     const uint32_t d_tmem = tmem + 256u + 128u * h, a_tmem = tmem + 128u * h;
@@ -232,7 +240,7 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
         const int row = lg * 32 + lane;     // row of the pipe = TMEM lane
         const uint32_t lane_addr = (uint32_t)(lg * 32) << 16;
         const uint32_t s_col = 128u * h, o_col = 256u + 128u * h;
-        const float sl2 = a.scale * 1.4426950408889634f;  // scores in base 2
+        const float sl2_base = a.scale * 1.4426950408889634f;  // scores in base 2
         uint32_t s_count = 0, epi_count = 0;
         bool ok = true;
         for (int64_t u = u_first; u * p.tiles_per_unit < g1; ++u) {
@@ -252,6 +260,9 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
                 continue;
             }
             const int n_ctx = context_len(a, s.b);
+            // fp8 cache: the unit's K scale joins the softmax scale, its V scale the normalisation
+            const float sl2 = FP8 ? sl2_base * __ldg(a.k_scale + (int64_t)s.b * a.Hkv + s.hk) : sl2_base;
+            const float vscale = FP8 ? __ldg(a.v_scale + (int64_t)s.b * a.Hkv + s.hk) : 1.f;
             float m_ref = -INFINITY, l = 0.f;
             IdxPair raw[4];  // sparse: index entries of this pipe's next tile, loaded one tile ahead
             if (SPARSE && warp_rows) {
@@ -384,7 +395,7 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
             ++epi_count;
             tc_fence_after();
             if (ok && warp_rows) {
-                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const float inv = l > 0.f ? vscale / l : 0.f;
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
                     uint32_t o[32];
@@ -415,8 +426,9 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
 
 // ---------------------------------------------------------------- host side
 
+// bf16 tiles in the 128-byte swizzle the tensor core reads, or (codes) unswizzled bytes.
 bool encode_map(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
-                const cuuint32_t *box) {
+                const cuuint32_t *box, bool codes = false) {
     static const PFN_cuTensorMapEncodeTiled_v12000 encode = [] {
         cudaDriverEntryPointQueryResult q;
         void *fn = nullptr;
@@ -428,8 +440,9 @@ bool encode_map(CUtensorMap *map, const void *base, int rank, const cuuint64_t *
     }();
     if (!encode) return false;
     cuuint32_t elem[4] = {1, 1, 1, 1};
-    CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), dims,
-                        strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    CUresult r = encode(map, codes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        (cuuint32_t)rank, const_cast<void *>(base), dims, strides, box, elem,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, codes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -437,7 +450,8 @@ bool encode_map(CUtensorMap *map, const void *base, int rank, const cuuint64_t *
 }  // namespace
 
 bool tc_supported(const VerifyArgs &a) {
-    if (a.kv_fp8) return false;  // the tensor-core tiles are bf16
+    // fp8 cache: the dense contiguous case (its codes are converted to bf16 tiles by the producer)
+    if (a.kv_fp8 && (a.idx || a.table)) return false;
     // the softmax takes the row max of the raw scores, which needs scale > 0
     if (!(a.G >= 1 && a.G <= 128 && (128 % a.G) == 0 && a.scale > 0.f)) return false;
     if (a.idx)  // gathered rows are copied 16 bytes at a time: every row start 16-byte aligned
@@ -461,6 +475,14 @@ cudaError_t launch_cache_attn_tc(const VerifyArgs &a, const SplitPlan &p, cudaSt
     if (sparse) {  // rows are gathered with cp.async; the K/V maps are not read
         mk = mq;
         mv = mq;
+    } else if (a.kv_fp8) {
+        // E4M3 codes [B, Hkv, L, d], one byte an element: 128 x 128-byte boxes into the staging,
+        // unswizzled (the warp converts them into the swizzled bf16 tile)
+        const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)a.L, (cuuint64_t)a.Hkv, (cuuint64_t)a.B};
+        const cuuint64_t strides[3] = {(cuuint64_t)a.st, (cuuint64_t)a.sh, (cuuint64_t)a.sb};
+        const cuuint32_t box[4] = {(cuuint32_t)D, (cuuint32_t)T, 1, 1};
+        if (!encode_map(&mk, a.k_cache, 4, dims, strides, box, true)) return cudaSuccess;
+        if (!encode_map(&mv, a.v_cache, 4, dims, strides, box, true)) return cudaSuccess;
     } else {
         // contiguous cache [B, Hkv, L, d] or (paged) the pool [blocks, Hkv, block_size, d]
         const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)(a.table ? a.block_size : a.L), (cuuint64_t)a.Hkv,
@@ -473,13 +495,17 @@ cudaError_t launch_cache_attn_tc(const VerifyArgs &a, const SplitPlan &p, cudaSt
     TcParams tp;
     tp.M = a.G * a.N;
     tp.split_tiles = tp.M <= 128 ? 1 : 0;
-    auto kern = sparse ? cache_attn_tc_kernel<true, false>
-                       : (a.table ? cache_attn_tc_kernel<false, true> : cache_attn_tc_kernel<false, false>);
+    auto kern = sparse ? cache_attn_tc_kernel<true, false, false>
+                : a.table  ? cache_attn_tc_kernel<false, true, false>
+                : a.kv_fp8 ? cache_attn_tc_kernel<false, false, true>
+                           : cache_attn_tc_kernel<false, false, false>;
     static PerDeviceOnce attr_once;
     cudaError_t e = once_per_device(attr_once, [] {
-        cudaError_t r = kernel_attributes(cache_attn_tc_kernel<false, false>, SMEM_BYTES);
-        if (r == cudaSuccess) r = kernel_attributes(cache_attn_tc_kernel<false, true>, SMEM_BYTES);
-        return r != cudaSuccess ? r : kernel_attributes(cache_attn_tc_kernel<true, false>, SMEM_BYTES);
+        cudaError_t r = cudaSuccess;
+        for (auto k : {cache_attn_tc_kernel<false, false, false>, cache_attn_tc_kernel<false, true, false>,
+                       cache_attn_tc_kernel<true, false, false>, cache_attn_tc_kernel<false, false, true>})
+            if (r == cudaSuccess) r = kernel_attributes(k, SMEM_BYTES);
+        return r;
     });
     if (e != cudaSuccess) return e;
     if (ev0) cudaEventRecord(ev0, s);

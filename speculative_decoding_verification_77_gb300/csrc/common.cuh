@@ -2,6 +2,8 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -226,6 +228,15 @@ struct VerifyArgs {
     const float *k_scale;
     const float *v_scale;
 };
+
+// Two E4M3 codes (the lower byte first) -> the bf16 pair of the same numbers (exact: E4M3 ->
+// f16 is exact, and so is f16 -> f32 -> bf16 for every E4M3 number).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+    const __nv_bfloat162 v = __floats2bfloat162_rn(f.x, f.y);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
 
 // Context length of sequence b, clamped to [0, L]; out-of-range values flag bad input.
 __device__ __forceinline__ int context_len(const VerifyArgs &a, int b) {
