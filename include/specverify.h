@@ -186,9 +186,11 @@ spec_status_t spec_verify_attn_sparse(const uint16_t *q, const uint16_t *k_cache
  * count bytes and must be multiples of 16). The value of element (b, h, t, c)
  * is the code's number times k_scale[b * Hkv + h] (v_scale for V): fp32
  * device arrays [B * Hkv], 4-byte aligned. Queries and the draft block stay
- * bf16. The fp8 cache runs on the warp-level tensor-core kernel, which
- * converts the codes to bf16 in shared memory (exact) and folds the scales
- * into the softmax scale and the partial's normalisation.
+ * bf16. The codes are converted to bf16 in shared memory (exact: every E4M3
+ * number is a bf16 number; a NaN code gives NaN) and the scales fold into the
+ * softmax scale and the partial's normalisation; dense contiguous caches with
+ * G a divisor of 128 run on the tcgen05 kernel, the other forms on the
+ * warp-level tensor-core kernel.
  * workspace: >= spec_verify_workspace_size(B, N, Hq, Hkv, d, idx ? budget : L).
  */
 typedef enum { SPEC_OUT_F32 = 0, SPEC_OUT_BF16 = 1 } spec_out_dtype_t;

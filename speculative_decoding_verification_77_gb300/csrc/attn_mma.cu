@@ -196,10 +196,7 @@ __global__ void __launch_bounds__(THREADS, 2) cache_attn_mma_kernel(VerifyArgs a
                     const uint4 codes = *reinterpret_cast<const uint4 *>(sK8 + kv * TILE8_BYTES + row * ROW8_BYTES + ch * 16);
                     uint8_t *dst = sKV + kv * TILE_BYTES;
                     uint4 lo, hi;
-                    lo.x = e4m3x2_to_bf16x2(codes.x & 0xffffu); lo.y = e4m3x2_to_bf16x2(codes.x >> 16);
-                    lo.z = e4m3x2_to_bf16x2(codes.y & 0xffffu); lo.w = e4m3x2_to_bf16x2(codes.y >> 16);
-                    hi.x = e4m3x2_to_bf16x2(codes.z & 0xffffu); hi.y = e4m3x2_to_bf16x2(codes.z >> 16);
-                    hi.z = e4m3x2_to_bf16x2(codes.w & 0xffffu); hi.w = e4m3x2_to_bf16x2(codes.w >> 16);
+                    e4m3x16_to_bf16x16(codes, lo, hi);
                     *reinterpret_cast<uint4 *>(dst + swz(row, 2 * ch)) = lo;
                     *reinterpret_cast<uint4 *>(dst + swz(row, 2 * ch + 1)) = hi;
                 }

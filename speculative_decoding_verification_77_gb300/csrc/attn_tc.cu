@@ -38,6 +38,11 @@
 // unit the pipes take rows 0-127 and 128-255 of every tile; with at most 128
 // rows they take alternate tiles of the same rows and each writes its own
 // partial. TMEM (512 columns): S_0, S_1, O_0, O_1, 128 columns each.
+// fp8 cache (dense, contiguous): the producer brings each K or V tile as
+// E4M3 codes by TMA into one of four staging buffers; warps 10 and 11 each
+// convert half of it into the bf16 ring (3 slots), fence the async proxy and
+// arrive on the slot and the staging buffer; the unit's K scale joins the
+// softmax scale and its V scale the final normalisation.
 // Every wait on an mbarrier is bounded; a wait that gives up records
 // SPEC_ERR_TIMEOUT, the CTA drains its in-flight copies and MMAs, frees TMEM
 // and returns.
@@ -57,6 +62,8 @@ constexpr int SMEM_BAR = SMEM_RING + RING * SLOT_BYTES;  // 229376
 constexpr int SMEM_BYTES = SMEM_BAR + 256 + 1024;        // + barriers + alignment slack
 constexpr int THREADS = 320;
 constexpr int WARP_PRODUCER = 8, WARP_MMA = 9;
+// fp8 cache: the converter warps follow the MMA warp
+constexpr int THREADS_FP8 = THREADS + 32 * FP8_CONVERTERS;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 128, true);
@@ -82,7 +89,7 @@ __device__ __forceinline__ void load_q(const CUtensorMap *tm_q, uint8_t *sQ, uin
 }
 
 template <bool SPARSE, bool PAGED, bool FP8>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(FP8 ? THREADS_FP8 : THREADS, 1)
 cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
                      const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v) {
@@ -92,8 +99,8 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint8_t *sQ = smem;
     uint8_t *sRing = smem + SMEM_RING;
-    // fp8 cache: a ring of RING - 1 bf16 tiles, then the staging of two items of codes
-    constexpr int KRING = FP8 ? RING - 1 : RING;
+    // fp8 cache: a ring of FP8_KR bf16 tiles, then the staging of FP8_STAGES tiles of codes
+    constexpr int KRING = FP8 ? FP8_KR : RING;
     uint8_t *sStage = sRing + KRING * SLOT_BYTES;
     Bars &bs = *reinterpret_cast<Bars *>(smem + SMEM_BAR);
 
@@ -107,7 +114,8 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
             mbar_init(&bs.q_empty[i], 1);
         }
         for (int i = 0; i < RING; ++i) {
-            mbar_init(&bs.kv_full[i], SPARSE ? 32 : 1);  // sparse: one arrival per gathering lane
+            // sparse: one arrival per gathering lane; fp8: one per converter warp
+            mbar_init(&bs.kv_full[i], SPARSE ? 32 : FP8 ? FP8_CONVERTERS : 1);
             mbar_init(&bs.kv_empty[i], 1);
         }
         for (int h = 0; h < 2; ++h) {
@@ -116,8 +124,10 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
             mbar_init(&bs.o_done[h], 1);
             mbar_init(&bs.o_empty[h], 4);
         }
-        mbar_init(&bs.st_full[0], 1);
-        mbar_init(&bs.st_full[1], 1);
+        for (int i = 0; i < FP8_STAGES; ++i) {
+            mbar_init(&bs.st_full[i], 1);
+            mbar_init(&bs.st_empty[i], FP8_CONVERTERS);
+        }
         mbar_init(&bs.mma_done, 1);
         bs.abort = 0;
         fence_mbar_init();
@@ -142,10 +152,14 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
         __syncwarp();
     } else if (warp == WARP_PRODUCER) {
         // ------------------------------------------------------------ TMA producer
-        if (FP8)
-            produce_dense_fp8(bs, sRing, sStage, &tm_q, &tm_k, &tm_v, a, p, split_tiles, u_first, g0, g1, lane, qload);
-        else if (lane == 0)
+        if (FP8) {
+            if (lane == 0) produce_dense_fp8(bs, sStage, &tm_q, &tm_k, &tm_v, a, p, split_tiles, u_first, g0, g1, qload);
+        } else if (lane == 0)
             produce_dense<PAGED>(bs, sRing, &tm_q, &tm_k, &tm_v, a, p, split_tiles, u_first, g0, g1, qload);
+        __syncwarp();
+    } else if (FP8 && warp > WARP_MMA) {
+        // ------------------------------------------------------------ fp8 converters
+        convert_items(bs, sRing, sStage, g0, g1, lane, warp - WARP_MMA - 1, a.status);
         __syncwarp();
     } else if (warp == WARP_MMA) {
         // ------------------------------------------------------------ MMA issuer
@@ -509,7 +523,7 @@ cudaError_t launch_cache_attn_tc(const VerifyArgs &a, const SplitPlan &p, cudaSt
     });
     if (e != cudaSuccess) return e;
     if (ev0) cudaEventRecord(ev0, s);
-    kern<<<p.ctas, THREADS, SMEM_BYTES, s>>>(a, p, tp, mq, mk, mv);
+    kern<<<p.ctas, a.kv_fp8 && !sparse && !a.table ? THREADS_FP8 : THREADS, SMEM_BYTES, s>>>(a, p, tp, mq, mk, mv);
     e = cudaGetLastError();
     if (ev1) cudaEventRecord(ev1, s);
     count_launches(1);

@@ -238,6 +238,19 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
+// Sixteen E4M3 codes (byte j of the uint4 = element j) -> sixteen bf16 of the same numbers,
+// elements 0-7 in lo and 8-15 in hi (exact for every code, NaN included).
+__device__ __forceinline__ void e4m3x16_to_bf16x16(const uint4 codes, uint4 &lo, uint4 &hi) {
+    lo.x = e4m3x2_to_bf16x2(codes.x & 0xffffu);
+    lo.y = e4m3x2_to_bf16x2(codes.x >> 16);
+    lo.z = e4m3x2_to_bf16x2(codes.y & 0xffffu);
+    lo.w = e4m3x2_to_bf16x2(codes.y >> 16);
+    hi.x = e4m3x2_to_bf16x2(codes.z & 0xffffu);
+    hi.y = e4m3x2_to_bf16x2(codes.z >> 16);
+    hi.z = e4m3x2_to_bf16x2(codes.w & 0xffffu);
+    hi.w = e4m3x2_to_bf16x2(codes.w >> 16);
+}
+
 // Context length of sequence b, clamped to [0, L]; out-of-range values flag bad input.
 __device__ __forceinline__ int context_len(const VerifyArgs &a, int b) {
     if (!a.ctx_lens) return a.L;

@@ -25,7 +25,8 @@ struct Bars {
     uint64_t q_full[2], q_empty[2];  // Q buffers (two only when the pipes share the rows)
     uint64_t kv_full[RING], kv_empty[RING];
     uint64_t s_full[2], p_full[2], o_done[2], o_empty[2];
-    uint64_t st_full[2];  // fp8 cache: the staged codes of an item have landed
+    uint64_t st_full[4];   // fp8 cache: the staged codes of an item have landed
+    uint64_t st_empty[4];  // fp8 cache: every converter has read the staged codes
     uint64_t mma_done;
     uint32_t tmem_base;
     uint32_t abort;
@@ -174,21 +175,27 @@ __device__ __forceinline__ void produce_sparse(Bars &bs, uint8_t *sRing, const C
     if (lane == 0) drain_q(bs, split_tiles, seg_i);
 }
 
-// fp8 cache: one K or V tile of E4M3 codes (128 rows of 128 codes, row r at r * 128) converted
-// by the 32 lanes of a warp into the bf16 tile the TMA would have written (two 16 KiB column
-// halves; row r of a half at r * 128 bytes, its 16-byte chunk q at (q ^ (r & 7)) * 16, the
-// 128-byte swizzle of a 1024-byte aligned tile).
-__device__ __forceinline__ void convert_e4m3_tile(const uint8_t *src, uint8_t *dst, int lane) {
-#pragma unroll 4
-    for (int k = 0; k < 32; ++k) {
+// fp8 cache: the producer warp only requests the codes; converter warps (10, 11) each turn
+// half of every staged tile into a slot of a ring of FP8_KR bf16 tiles. The staging
+// (FP8_STAGES tiles of codes, 16 KiB each) takes the room of the bf16 ring's other slots.
+constexpr int FP8_CONVERTERS = 2;
+constexpr int FP8_KR = 3;
+constexpr int FP8_STAGES = 4;
+static_assert(2 * FP8_KR + FP8_STAGES <= 2 * RING, "fp8 ring and staging fit the bf16 ring's room");
+
+// fp8 cache: part `part` of FP8_CONVERTERS of one K or V tile of E4M3 codes (128 rows of 128
+// codes, row r at r * 128) converted by the 32 lanes of a warp into the bf16 tile the TMA
+// would have written (two 16 KiB column halves; row r of a half at r * 128 bytes, its 16-byte
+// chunk q at (q ^ (r & 7)) * 16, the 128-byte swizzle of a 1024-byte aligned tile). Part p
+// takes the 16-code chunks lane + 32 k for k = p, p + FP8_CONVERTERS, ...
+__device__ __forceinline__ void convert_e4m3_tile(const uint8_t *src, uint8_t *dst, int lane, int part) {
+#pragma unroll 2
+    for (int k = part; k < 32; k += FP8_CONVERTERS) {
         const int c = lane + 32 * k;  // 16 codes: row c >> 3, columns 16 (c & 7) .. + 15
         const int r = c >> 3, m = c & 7;
         const uint4 codes = *reinterpret_cast<const uint4 *>(src + c * 16);
         uint4 lo, hi;
-        lo.x = e4m3x2_to_bf16x2(codes.x & 0xffffu); lo.y = e4m3x2_to_bf16x2(codes.x >> 16);
-        lo.z = e4m3x2_to_bf16x2(codes.y & 0xffffu); lo.w = e4m3x2_to_bf16x2(codes.y >> 16);
-        hi.x = e4m3x2_to_bf16x2(codes.z & 0xffffu); hi.y = e4m3x2_to_bf16x2(codes.z >> 16);
-        hi.z = e4m3x2_to_bf16x2(codes.w & 0xffffu); hi.w = e4m3x2_to_bf16x2(codes.w >> 16);
+        e4m3x16_to_bf16x16(codes, lo, hi);
         uint8_t *row = dst + (m >> 2) * HALF_BYTES + r * 128;
         const int q0 = 2 * (m & 3);
         *reinterpret_cast<uint4 *>(row + ((q0 ^ (r & 7)) << 4)) = lo;
@@ -196,37 +203,45 @@ __device__ __forceinline__ void convert_e4m3_tile(const uint8_t *src, uint8_t *d
     }
 }
 
-// fp8 producer (the whole warp): lane 0 brings the E4M3 codes of every K and V tile of the
-// CTA's range by TMA into two staging buffers, two items ahead; the warp converts each item
-// into the next slot of a ring of RING - 1 bf16 tiles (the staging takes the last slot's
-// room), fences the generic-proxy stores for the tensor core and signals the slot. Item n of
-// the range is tile g0 + n / 2 (K for even n, V for odd), found from n alone. Each unit's Q
-// comes through qload(seg, buffer, bar) as in the bf16 producer.
+// fp8 cache: a converter warp, part `part` of every item of the CTA's range (item n: K of tile
+// g0 + n / 2 for even n, V for odd). Per item: wait for its staged codes and its ring slot,
+// convert, fence the generic-proxy stores for the tensor core, and (lane 0) arrive on the slot
+// and on the staging buffer.
+__device__ __forceinline__ void convert_items(Bars &bs, uint8_t *sRing, const uint8_t *sStage, int64_t g0, int64_t g1,
+                                              int lane, int part, uint32_t *status) {
+    const int64_t nitems = 2 * (g1 - g0);
+    for (int64_t n = 0; n < nitems; ++n) {
+        const int sb = (int)(n % FP8_STAGES);
+        if (!__all_sync(0xffffffffu, wait_bar(bs, &bs.st_full[sb], (uint32_t)((n / FP8_STAGES) & 1), status))) break;
+        const int slot = (int)(n % FP8_KR);
+        const int64_t use = n / FP8_KR;
+        if (use > 0 &&
+            !__all_sync(0xffffffffu, wait_bar(bs, &bs.kv_empty[slot], (uint32_t)((use - 1) & 1), status)))
+            break;
+        convert_e4m3_tile(sStage + sb * (T * kHeadDim), sRing + slot * SLOT_BYTES, lane, part);
+        fence_proxy_async_smem();  // the tensor core reads what these generic stores wrote
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(&bs.kv_full[slot]);
+            mbar_arrive(&bs.st_empty[sb]);
+        }
+    }
+}
+
+// fp8 producer (one thread): the E4M3 codes of every K and V tile of the CTA's range by TMA
+// into FP8_STAGES staging buffers (item m into buffer m % FP8_STAGES, once every converter
+// has arrived on that buffer's st_empty for item m - FP8_STAGES), and each unit's Q through
+// qload(seg, buffer, bar) before the unit's first item.
 template <class QLoad>
-__device__ __forceinline__ void produce_dense_fp8(Bars &bs, uint8_t *sRing, uint8_t *sStage, const CUtensorMap *tm_q,
+__device__ __forceinline__ void produce_dense_fp8(Bars &bs, uint8_t *sStage, const CUtensorMap *tm_q,
                                                   const CUtensorMap *tm_k, const CUtensorMap *tm_v, const VerifyArgs &a,
                                                   const SplitPlan &p, int split_tiles, int64_t u_first, int64_t g0,
-                                                  int64_t g1, int lane, QLoad qload) {
-    constexpr int KR = RING - 1;
+                                                  int64_t g1, QLoad qload) {
     constexpr uint32_t STAGE_BYTES = T * kHeadDim;  // 16 KiB of codes
-    const int64_t nitems = 2 * (g1 - g0);
-    auto issue = [&](int64_t n) {  // lane 0: the codes of item n into staging buffer n % 2
-        const int64_t g = g0 + n / 2;
-        const int64_t u = g / p.tiles_per_unit;
-        const int t = (int)(g - u * p.tiles_per_unit);
-        const int hk = (int)((u / p.row_groups) % a.Hkv);
-        const int b = (int)(u / ((int64_t)p.row_groups * a.Hkv));
-        uint64_t *bar = &bs.st_full[n & 1];
-        mbar_arrive_expect_tx(bar, STAGE_BYTES);
-        tma_load_4d(sStage + (n & 1) * STAGE_BYTES, (n & 1) ? tm_v : tm_k, bar, 0, t * T, hk, b);
-    };
-    if (lane == 0) {
-        tma_prefetch_desc(tm_q);
-        tma_prefetch_desc(tm_k);
-        tma_prefetch_desc(tm_v);
-        for (int64_t n = 0; n < 2 && n < nitems; ++n) issue(n);
-    }
-    int64_t n = 0;  // items converted so far
+    tma_prefetch_desc(tm_q);
+    tma_prefetch_desc(tm_k);
+    tma_prefetch_desc(tm_v);
+    int64_t m = 0;  // items requested so far
     int q_loads = 0;
     bool ok = true;
     for (int64_t u = u_first; ok && u * p.tiles_per_unit < g1; ++u, ++q_loads) {
@@ -235,33 +250,24 @@ __device__ __forceinline__ void produce_dense_fp8(Bars &bs, uint8_t *sRing, uint
         int qb;
         uint32_t quse;
         q_buffer(split_tiles, q_loads, qb, quse);
-        if (quse > 0 && !(ok = __all_sync(0xffffffffu, wait_bar(bs, &bs.q_empty[qb], (quse - 1) & 1, a.status)))) break;
-        if (lane == 0) qload(s, qb, &bs.q_full[qb]);
+        if (quse > 0 && !(ok = wait_bar(bs, &bs.q_empty[qb], (quse - 1) & 1, a.status))) break;
+        qload(s, qb, &bs.q_full[qb]);
         for (int t = s.tb; ok && t < s.te; ++t) {
-            for (int kv = 0; kv < 2; ++kv, ++n) {
-                const int st = (int)(n & 1);
-                if (!(ok = __all_sync(0xffffffffu, wait_bar(bs, &bs.st_full[st], (uint32_t)((n >> 1) & 1), a.status))))
+            for (int kv = 0; kv < 2; ++kv, ++m) {
+                const int sb = (int)(m % FP8_STAGES);
+                if (m >= FP8_STAGES &&
+                    !(ok = wait_bar(bs, &bs.st_empty[sb], (uint32_t)((m / FP8_STAGES - 1) & 1), a.status)))
                     break;
-                const int slot = (int)(n % KR);
-                const int64_t use = n / KR;
-                if (use > 0 &&
-                    !(ok = __all_sync(0xffffffffu, wait_bar(bs, &bs.kv_empty[slot], (uint32_t)((use - 1) & 1), a.status))))
-                    break;
-                convert_e4m3_tile(sStage + st * STAGE_BYTES, sRing + slot * SLOT_BYTES, lane);
-                fence_proxy_async_smem();  // the tensor core reads what these generic stores wrote
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&bs.kv_full[slot]);
-                    if (n + 2 < nitems) issue(n + 2);  // the staging buffer is free again
-                }
+                uint64_t *bar = &bs.st_full[sb];
+                mbar_arrive_expect_tx(bar, STAGE_BYTES);
+                tma_load_4d(sStage + sb * STAGE_BYTES, kv ? tm_v : tm_k, bar, 0, t * T, s.hk, s.b);
             }
         }
     }
-    // the drain: a load issued two items ahead that was never converted (a wait gave up)
-    if (lane == 0) {
-        for (int64_t m = n; m < nitems && m < n + 2; ++m) drain_wait(&bs.st_full[m & 1], (uint32_t)((m >> 1) & 1));
-        drain_q(bs, split_tiles, q_loads);
-    }
+    // the drain: the last FP8_STAGES loads (one per buffer) have landed before the CTA ends
+    for (int64_t i = m > FP8_STAGES ? m - FP8_STAGES : 0; i < m; ++i)
+        drain_wait(&bs.st_full[i % FP8_STAGES], (uint32_t)((i / FP8_STAGES) & 1));
+    drain_q(bs, split_tiles, q_loads);
 }
 
 // TMA producer (one thread): the K and V tiles of the CTA's range, and each

@@ -805,6 +805,54 @@ def test_fp8_cache_matches_oracle(ops, case):
         assert_attn_close(out, lse, ro, rl, rows)
 
 
+@pytest.mark.parametrize("path", ["tcgen05", "portable"])
+def test_fp8_every_code_converts_exactly(ops, path):
+    """Caches drawn uniformly from the 254 finite E4M3 codes (zeros of both signs, every
+    subnormal, the largest numbers) on the tensor-core kernel (G = 4) and on the warp-level one
+    (G = 3): both convert the codes to bf16 without error, so the result is the oracle's."""
+    Hq, Hkv = (8, 2) if path == "tcgen05" else (12, 4)
+    B, N, L = 2, 6, 700
+    x = small(41 if path == "tcgen05" else 43, B=B, N=N, Hq=Hq, Hkv=Hkv, L=L)
+    gen = torch.Generator().manual_seed(17)
+    finite = torch.tensor([c for c in range(256) if c & 0x7F != 0x7F], dtype=torch.uint8)
+    pick = lambda: finite[torch.randint(0, len(finite), (B, Hkv, L, 128), generator=gen)].view(torch.float8_e4m3fn)
+    kc, vc = pick(), pick()
+    ks = torch.full((B, Hkv), 1.0 / (448 * 8), dtype=torch.float32)
+    vs = (torch.rand(B, Hkv, generator=gen) + 0.5).float() / 448
+    g = to_dev(x)
+    out, lse = ops.verify_attn_ex(g["q"], kc.to(dev()), vc.to(dev()), g["k_draft"], g["v_draft"], g["parent"],
+                                  scale=x["scale"], k_scale=ks.to(dev()), v_scale=vs.to(dev()))
+    ro, rl, st = oracle.attend_fp8(x["q"], kc, vc, ks, vs, x["k_draft"], x["v_draft"], x["parent"], scale=x["scale"])
+    assert st == 0
+    torch.cuda.synchronize()
+    assert_attn_close(out, lse, ro, rl)
+
+
+@pytest.mark.parametrize("path", ["tcgen05", "portable"])
+def test_fp8_nan_code_in_v_gives_nan_columns(ops, path):
+    """A NaN code in V (0x7F or 0xFF) is a NaN in the output column it sits in, for every query
+    row of that KV head, as in the oracle; everything else is unchanged."""
+    Hq, Hkv = (8, 2) if path == "tcgen05" else (12, 4)
+    B, N, L = 2, 4, 600
+    x = small(47, B=B, N=N, Hq=Hq, Hkv=Hkv, L=L)
+    kc, ks = quantize_e4m3(x["k_cache"])
+    vc, vs = quantize_e4m3(x["v_cache"])
+    vb = vc.view(torch.uint8).clone()
+    vb[0, 1, 500, 7] = 0x7F
+    vb[1, 0, 3, 100] = 0xFF
+    vc = vb.view(torch.float8_e4m3fn)
+    g = to_dev(x)
+    out, lse = ops.verify_attn_ex(g["q"], kc.to(dev()), vc.to(dev()), g["k_draft"], g["v_draft"], g["parent"],
+                                  scale=x["scale"], k_scale=ks.to(dev()), v_scale=vs.to(dev()))
+    ro, rl, st = oracle.attend_fp8(x["q"], kc, vc, ks, vs, x["k_draft"], x["v_draft"], x["parent"], scale=x["scale"])
+    torch.cuda.synchronize()
+    o = out.cpu().numpy().reshape(ro.shape)
+    nan = np.isnan(ro)
+    assert nan.any() and np.array_equal(np.isnan(o), nan)
+    assert np.abs(o[~nan] - ro[~nan]).max() <= ATOL_O
+    assert np.all(np.isfinite(lse.cpu().numpy())) and np.abs(lse.cpu().numpy().reshape(-1) - rl).max() <= ATOL_L
+
+
 def test_importance_scores_headline_shape(ops):
     """The headline layer (B=4, L=32k, N=64 tree) scored on two heads of different KV heads,
     against the oracle on a sample of tokens of every sequence (all draft queries of each)."""
