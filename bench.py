@@ -474,7 +474,7 @@ def time_lse_merge(dev, stream, args, peaks, peak_src, windows):
 def time_fp8(dev, stream, args, peaks, peak_src, windows):
     """The headline layer (B=4, L=32k, N=64 tree) over an fp8 cache: the bf16 cache quantised to
     E4M3 codes with a scale per (sequence, KV head), verified through spec_verify_attn_ex (the
-    tcgen05 kernel loads the codes by TMA and two warps convert them into its bf16 tiles).
+    tcgen05 kernel loads the codes by TMA and six warps convert them into its bf16 tiles).
     Algorithmic bytes: the codes, 1 B an element (268 MB)."""
     from speculative_decoding_verification_77_gb300 import ops
 
@@ -508,7 +508,7 @@ def time_fp8(dev, stream, args, peaks, peak_src, windows):
     gbs = nbytes / (ms * 1e-3) / 1e9
     e = {"workload": w.name + " over an E4M3 cache (scale per sequence and KV head)", "us_per_step": round(ms * 1e3, 2),
          "kv_bytes_per_step": nbytes, "achieved_gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
-         "kernel": "cache_attn_tc<fp8> (codes by TMA, converted to bf16 tiles by two warps) + merge",
+         "kernel": "cache_attn_tc<fp8> (codes by TMA, converted to bf16 tiles by six warps) + merge",
          "l2": "inputs larger than L2, no flush", "peaks": f"{peak_src}: hbm {peaks['hbm_gbs']} GB/s",
          "steps_timed": len(v)}
     windows.append((e, t0, t1))

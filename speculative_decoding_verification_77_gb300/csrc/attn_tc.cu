@@ -38,11 +38,12 @@
 // unit the pipes take rows 0-127 and 128-255 of every tile; with at most 128
 // rows they take alternate tiles of the same rows and each writes its own
 // partial. TMEM (512 columns): S_0, S_1, O_0, O_1, 128 columns each.
-// fp8 cache (dense, contiguous): the producer brings each K or V tile as
-// E4M3 codes by TMA into one of four staging buffers; warps 10 and 11 each
-// convert half of it into the bf16 ring (3 slots), fence the async proxy and
-// arrive on the slot and the staging buffer; the unit's K scale joins the
-// softmax scale and its V scale the final normalisation.
+// fp8 cache (dense, contiguous; 512 threads): the producer brings each K or
+// V tile as E4M3 codes by TMA into one of four staging buffers; warps 10-15
+// each convert a sixth of it into the bf16 ring (3 slots), fence the async
+// proxy and arrive on the slot and the staging buffer; the unit's K scale
+// joins the softmax scale and its V scale the final normalisation. Warps 8-15
+// give registers back (setmaxnreg) to the two softmax warpgroups.
 // Every wait on an mbarrier is bounded; a wait that gives up records
 // SPEC_ERR_TIMEOUT, the CTA drains its in-flight copies and MMAs, frees TMEM
 // and returns.
@@ -64,6 +65,10 @@ constexpr int THREADS = 320;
 constexpr int WARP_PRODUCER = 8, WARP_MMA = 9;
 // fp8 cache: the converter warps follow the MMA warp
 constexpr int THREADS_FP8 = THREADS + 32 * FP8_CONVERTERS;
+// 512 threads start with 128 registers each; two warpgroups at 176 and two at 80 use them all
+constexpr uint32_t FP8_REGS_SOFTMAX = 176, FP8_REGS_OTHER = 80;
+static_assert(THREADS_FP8 == 512 && 256 * (FP8_REGS_SOFTMAX + FP8_REGS_OTHER) == 65536,
+              "the register split adds up to the launch's registers");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 128, true);
@@ -146,108 +151,113 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
 
     // Q of a unit into buffer qb (one thread)
     auto qload = [&](const Seg &sg, int qb, uint64_t *bar) { load_q(&tm_q, sQ, bar, split_tiles, qb, sg, BM, a.G, a.N); };
-    if (SPARSE && warp == WARP_PRODUCER) {
-        // ------------------------------------------------------------ gather producer
-        produce_sparse(bs, sRing, &tm_q, a, p, split_tiles, u_first, g0, g1, lane, qload);
-        __syncwarp();
-    } else if (warp == WARP_PRODUCER) {
-        // ------------------------------------------------------------ TMA producer
-        if (FP8) {
-            if (lane == 0) produce_dense_fp8(bs, sStage, &tm_q, &tm_k, &tm_v, a, p, split_tiles, u_first, g0, g1, qload);
-        } else if (lane == 0)
-            produce_dense<PAGED>(bs, sRing, &tm_q, &tm_k, &tm_v, a, p, split_tiles, u_first, g0, g1, qload);
-        __syncwarp();
-    } else if (FP8 && warp > WARP_MMA) {
-        // ------------------------------------------------------------ fp8 converters
-        convert_items(bs, sRing, sStage, g0, g1, lane, warp - WARP_MMA - 1, a.status);
-        __syncwarp();
-    } else if (warp == WARP_MMA) {
-        // ------------------------------------------------------------ MMA issuer
-        // The whole warp runs the issue loop (its operands stay warp-uniform); one elected
-        // lane issues each tcgen05 instruction.
-        {
-            uint32_t item_base = 0;
-            int seg_i = 0;
-            uint32_t pv_count[2] = {0, 0};   // PV MMAs issued per pipe
-            uint32_t pipe_segs[2] = {0, 0};  // segments in which the pipe produced a partial
-            bool ok = true;
-            // Descriptors are built once; every MMA only adds compile-time offsets (16-byte
-            // units), which keeps the single issuing thread's instruction stream short.
-            const uint64_t dq_base = desc_sw128(smem_u32(sQ), 16, 1024);
-            const uint64_t dk0 = desc_sw128(smem_u32(sRing), 16, 1024);
-            const uint64_t dv0 = desc_sw128(smem_u32(sRing), 16384, 1024);
-            for (int64_t u = u_first; ok && u * p.tiles_per_unit < g1; ++u, ++seg_i) {
-                Seg s;
-                seg_decode(a, p, split_tiles, u, g0, g1, s);
-                int qb;
-                uint32_t quse;
-                q_buffer(split_tiles, seg_i, qb, quse);
-                if (!(ok = __all_sync(0xffffffffu, wait_bar(bs, &bs.q_full[qb], quse & 1, a.status)))) break;
-                // Q of pipe h: its own 128-row block (more than 128 rows) or this unit's buffer
-                const uint64_t dq0 = dq_base + (split_tiles ? (uint64_t)qb * (16384u >> 4) : 0u);
-                const uint64_t dq1 = split_tiles ? dq0 : dq_base + (16384u >> 4);
-                tc_fence_after();
-                const int qk_total = s.cnt[0] + s.cnt[1];
-                int qk_done = 0;
-                auto issue_qk = [&](int h, int i) -> bool {
-                    const uint32_t n = item_base + 2u * (uint32_t)(seg_tile(s, split_tiles, h, i) - s.tb);
-                    const uint32_t slot = n % KRING;
-                    // pipe 1 of a shared tile reuses the K tile pipe 0 already waited for
-                    if ((split_tiles || h == 0) && !__all_sync(0xffffffffu, wait_bar(bs, &bs.kv_full[slot], (n / KRING) & 1u, a.status)))
-                        return false;
-                    if (SPARSE || FP8) fence_proxy_async_smem();  // the slot was written by the generic proxy
-                    const uint64_t dq = h ? dq1 : dq0;
-                    const uint64_t dk = dk0 + (uint64_t)slot * (SLOT_BYTES >> 4);
-                    const uint32_t d_tmem = tmem + 128u * h;
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        mma_ss_elect(d_tmem, dq + (uint64_t)((ks >> 2) * 2048 + (ks & 3) * 2),
-                               dk + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2), IDESC_QK, ks > 0 ? 1u : 0u);
-                    mma_commit_elect(&bs.s_full[h]);
-                    if (split_tiles || h == 1) mma_commit_elect(&bs.kv_empty[slot]);
-                    if (++qk_done == qk_total) mma_commit_elect(&bs.q_empty[qb]);
-                    return true;
-                };
-                auto issue_pv = [&](int h, int i) -> bool {
-                    if (!__all_sync(0xffffffffu, wait_bar(bs, &bs.p_full[h], pv_count[h] & 1, a.status))) return false;
-                    if (i == 0 && pipe_segs[h] > 0 &&
-                        !__all_sync(0xffffffffu, wait_bar(bs, &bs.o_empty[h], (pipe_segs[h] - 1) & 1, a.status)))
-                        return false;
-                    const uint32_t n = item_base + 2u * (uint32_t)(seg_tile(s, split_tiles, h, i) - s.tb) + 1u;
-                    const uint32_t slot = n % KRING;
-                    if ((split_tiles || h == 0) && !__all_sync(0xffffffffu, wait_bar(bs, &bs.kv_full[slot], (n / KRING) & 1u, a.status)))
-                        return false;
-                    if (SPARSE || FP8) fence_proxy_async_smem();  // the slot was written by the generic proxy
-                    tc_fence_after();  // P_h was written to TMEM by the softmax warps
-                    const uint64_t dv = dv0 + (uint64_t)slot * (SLOT_BYTES >> 4);
-                    const uint32_t d_tmem = tmem + 256u + 128u * h, a_tmem = tmem + 128u * h;
-                    const uint32_t acc0 = i > 0 ? 1u : 0u;
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        mma_ts_elect(d_tmem, a_tmem + 8u * ks, dv + (uint64_t)(ks * 128), IDESC_PV, ks > 0 ? 1u : acc0);
-                    if (split_tiles || h == 1) mma_commit_elect(&bs.kv_empty[slot]);
-                    if (i == s.cnt[h] - 1) mma_commit_elect(&bs.o_done[h]);  // the unit's O_h is final
-                    ++pv_count[h];
-                    return true;
-                };
-                for (int h = 0; ok && h < 2; ++h)
-                    if (s.cnt[h] > 0) ok = issue_qk(h, 0);
-                const int n_iter = s.cnt[0];
-                for (int i = 0; ok && i < n_iter; ++i)
-                    for (int h = 0; ok && h < 2; ++h) {
-                        if (i >= s.cnt[h]) continue;
-                        ok = issue_pv(h, i);
-                        if (ok && i + 1 < s.cnt[h]) ok = issue_qk(h, i + 1);
-                    }
-                for (int h = 0; h < 2; ++h)
-                    if (s.cnt[h] > 0) ++pipe_segs[h];
-                item_base += 2u * (uint32_t)(s.te - s.tb);
+    if (warp >= WARP_PRODUCER) {
+        // fp8: this warpgroup and the next (loader, issuer, converters) give registers to the softmax
+        if (FP8) setmaxnreg_dec<FP8_REGS_OTHER>();
+        if (SPARSE && warp == WARP_PRODUCER) {
+            // ------------------------------------------------------------ gather producer
+            produce_sparse(bs, sRing, &tm_q, a, p, split_tiles, u_first, g0, g1, lane, qload);
+            __syncwarp();
+        } else if (warp == WARP_PRODUCER) {
+            // ------------------------------------------------------------ TMA producer
+            if (FP8) {
+                if (lane == 0) produce_dense_fp8(bs, sStage, &tm_q, &tm_k, &tm_v, a, p, split_tiles, u_first, g0, g1, qload);
+            } else if (lane == 0)
+                produce_dense<PAGED>(bs, sRing, &tm_q, &tm_k, &tm_v, a, p, split_tiles, u_first, g0, g1, qload);
+            __syncwarp();
+        } else if (FP8 && warp > WARP_MMA) {
+            // ------------------------------------------------------------ fp8 converters
+            convert_items(bs, sRing, sStage, g0, g1, lane, warp - WARP_MMA - 1, a.status);
+            __syncwarp();
+        } else if (warp == WARP_MMA) {
+            // ------------------------------------------------------------ MMA issuer
+            // The whole warp runs the issue loop (its operands stay warp-uniform); one elected
+            // lane issues each tcgen05 instruction.
+            {
+                uint32_t item_base = 0;
+                int seg_i = 0;
+                uint32_t pv_count[2] = {0, 0};   // PV MMAs issued per pipe
+                uint32_t pipe_segs[2] = {0, 0};  // segments in which the pipe produced a partial
+                bool ok = true;
+                // Descriptors are built once; every MMA only adds compile-time offsets (16-byte
+                // units), which keeps the single issuing thread's instruction stream short.
+                const uint64_t dq_base = desc_sw128(smem_u32(sQ), 16, 1024);
+                const uint64_t dk0 = desc_sw128(smem_u32(sRing), 16, 1024);
+                const uint64_t dv0 = desc_sw128(smem_u32(sRing), 16384, 1024);
+                for (int64_t u = u_first; ok && u * p.tiles_per_unit < g1; ++u, ++seg_i) {
+                    Seg s;
+                    seg_decode(a, p, split_tiles, u, g0, g1, s);
+                    int qb;
+                    uint32_t quse;
+                    q_buffer(split_tiles, seg_i, qb, quse);
+                    if (!(ok = __all_sync(0xffffffffu, wait_bar(bs, &bs.q_full[qb], quse & 1, a.status)))) break;
+                    // Q of pipe h: its own 128-row block (more than 128 rows) or this unit's buffer
+                    const uint64_t dq0 = dq_base + (split_tiles ? (uint64_t)qb * (16384u >> 4) : 0u);
+                    const uint64_t dq1 = split_tiles ? dq0 : dq_base + (16384u >> 4);
+                    tc_fence_after();
+                    const int qk_total = s.cnt[0] + s.cnt[1];
+                    int qk_done = 0;
+                    auto issue_qk = [&](int h, int i) -> bool {
+                        const uint32_t n = item_base + 2u * (uint32_t)(seg_tile(s, split_tiles, h, i) - s.tb);
+                        const uint32_t slot = n % KRING;
+                        // pipe 1 of a shared tile reuses the K tile pipe 0 already waited for
+                        if ((split_tiles || h == 0) && !__all_sync(0xffffffffu, wait_bar(bs, &bs.kv_full[slot], (n / KRING) & 1u, a.status)))
+                            return false;
+                        if (SPARSE || FP8) fence_proxy_async_smem();  // the slot was written by the generic proxy
+                        const uint64_t dq = h ? dq1 : dq0;
+                        const uint64_t dk = dk0 + (uint64_t)slot * (SLOT_BYTES >> 4);
+                        const uint32_t d_tmem = tmem + 128u * h;
+    #pragma unroll
+                        for (int ks = 0; ks < 8; ++ks)
+                            mma_ss_elect(d_tmem, dq + (uint64_t)((ks >> 2) * 2048 + (ks & 3) * 2),
+                                   dk + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2), IDESC_QK, ks > 0 ? 1u : 0u);
+                        mma_commit_elect(&bs.s_full[h]);
+                        if (split_tiles || h == 1) mma_commit_elect(&bs.kv_empty[slot]);
+                        if (++qk_done == qk_total) mma_commit_elect(&bs.q_empty[qb]);
+                        return true;
+                    };
+                    auto issue_pv = [&](int h, int i) -> bool {
+                        if (!__all_sync(0xffffffffu, wait_bar(bs, &bs.p_full[h], pv_count[h] & 1, a.status))) return false;
+                        if (i == 0 && pipe_segs[h] > 0 &&
+                            !__all_sync(0xffffffffu, wait_bar(bs, &bs.o_empty[h], (pipe_segs[h] - 1) & 1, a.status)))
+                            return false;
+                        const uint32_t n = item_base + 2u * (uint32_t)(seg_tile(s, split_tiles, h, i) - s.tb) + 1u;
+                        const uint32_t slot = n % KRING;
+                        if ((split_tiles || h == 0) && !__all_sync(0xffffffffu, wait_bar(bs, &bs.kv_full[slot], (n / KRING) & 1u, a.status)))
+                            return false;
+                        if (SPARSE || FP8) fence_proxy_async_smem();  // the slot was written by the generic proxy
+                        tc_fence_after();  // P_h was written to TMEM by the softmax warps
+                        const uint64_t dv = dv0 + (uint64_t)slot * (SLOT_BYTES >> 4);
+                        const uint32_t d_tmem = tmem + 256u + 128u * h, a_tmem = tmem + 128u * h;
+                        const uint32_t acc0 = i > 0 ? 1u : 0u;
+    #pragma unroll
+                        for (int ks = 0; ks < 8; ++ks)
+                            mma_ts_elect(d_tmem, a_tmem + 8u * ks, dv + (uint64_t)(ks * 128), IDESC_PV, ks > 0 ? 1u : acc0);
+                        if (split_tiles || h == 1) mma_commit_elect(&bs.kv_empty[slot]);
+                        if (i == s.cnt[h] - 1) mma_commit_elect(&bs.o_done[h]);  // the unit's O_h is final
+                        ++pv_count[h];
+                        return true;
+                    };
+                    for (int h = 0; ok && h < 2; ++h)
+                        if (s.cnt[h] > 0) ok = issue_qk(h, 0);
+                    const int n_iter = s.cnt[0];
+                    for (int i = 0; ok && i < n_iter; ++i)
+                        for (int h = 0; ok && h < 2; ++h) {
+                            if (i >= s.cnt[h]) continue;
+                            ok = issue_pv(h, i);
+                            if (ok && i + 1 < s.cnt[h]) ok = issue_qk(h, i + 1);
+                        }
+                    for (int h = 0; h < 2; ++h)
+                        if (s.cnt[h] > 0) ++pipe_segs[h];
+                    item_base += 2u * (uint32_t)(s.te - s.tb);
+                }
+                // drain: every MMA issued so far must complete before TMEM is freed
+                mma_commit_elect(&bs.mma_done);
+                drain_wait(&bs.mma_done, 0);
             }
-            // drain: every MMA issued so far must complete before TMEM is freed
-            mma_commit_elect(&bs.mma_done);
-            drain_wait(&bs.mma_done, 0);
         }
     } else {
+        if (FP8) setmaxnreg_inc<FP8_REGS_SOFTMAX>();
         // ------------------------------------------------------------ softmax warps
         const int h = warp >> 2;            // pipe
         const int lg = warp & 3;            // TMEM lane group of this warp

@@ -175,10 +175,10 @@ __device__ __forceinline__ void produce_sparse(Bars &bs, uint8_t *sRing, const C
     if (lane == 0) drain_q(bs, split_tiles, seg_i);
 }
 
-// fp8 cache: the producer warp only requests the codes; converter warps (10, 11) each turn
-// half of every staged tile into a slot of a ring of FP8_KR bf16 tiles. The staging
+// fp8 cache: the producer warp only requests the codes; converter warps (10-15) each turn
+// a sixth of every staged tile into a slot of a ring of FP8_KR bf16 tiles. The staging
 // (FP8_STAGES tiles of codes, 16 KiB each) takes the room of the bf16 ring's other slots.
-constexpr int FP8_CONVERTERS = 2;
+constexpr int FP8_CONVERTERS = 6;
 constexpr int FP8_KR = 3;
 constexpr int FP8_STAGES = 4;
 static_assert(2 * FP8_KR + FP8_STAGES <= 2 * RING, "fp8 ring and staging fit the bf16 ring's room");
