@@ -51,11 +51,11 @@ SWEEP_N = (1, 4, 16, 64, 256)
 # capture, keyed by the sha256 of the kernel sources it was taken on and the
 # workload; a changed kernel reports null.
 NCU_TRAFFIC = {
-    ("68eecf5f6cb9cb11", "llama3-8b-layer-B4-L32k-N64-tree"): 540_649_728 + 8_762_368,
-    ("68eecf5f6cb9cb11", "sparse-hybrid-B16-L32k-k2048-N8-chain"): 136_131_072 + 6_466_560,
-    # captured at L = 32k (1.08 GB of reads, 12.6 MB of partials written): reads scaled by 4
-    ("68eecf5f6cb9cb11", "qwen2.5-72b-layer-B8-L128k-N32-tree"): 4 * 1_081_532_000 + 12_563_968,
-    ("68eecf5f6cb9cb11", "tree-sweep-B8-L16k-N256-best-first"): 2_173_974_000 + 39_198_720,
+    ("72e5ea4f87ab482b", "llama3-8b-layer-B4-L32k-N64-tree"): 540_644_864 + 8_768_256,
+    ("72e5ea4f87ab482b", "sparse-hybrid-B16-L32k-k2048-N8-chain"): 135_792_128 + 5_909_504,
+    # captured at L = 32k (1.08 GB of reads, 12.7 MB of partials written): reads scaled by 4
+    ("72e5ea4f87ab482b", "qwen2.5-72b-layer-B8-L128k-N32-tree"): 4 * 1_081_531_000 + 12_724_736,
+    ("72e5ea4f87ab482b", "tree-sweep-B8-L16k-N256-best-first"): 2_174_109_000 + 39_266_048,
 }
 NCU_TRAFFIC_NOTE = {
     "qwen2.5-72b-layer-B8-L128k-N32-tree": "from an ncu capture at L=32k: K/V reads x4 (they grow with L), "
