@@ -21,8 +21,9 @@
 // shared memory (two 16-bit counts per word), and after the barrier every CTA
 // reads the CL histograms of the cluster through distributed shared memory (one
 // 8-byte read per peer and thread, 4 bins) and finds the same digit from the
-// same totals, with no further exchange. The histograms alternate between two
-// buffers, so a pass never overwrites a buffer that a peer may still be reading.
+// same totals, with two CTA barriers and no further exchange. The histograms
+// alternate between two buffers, so a pass never overwrites a buffer that a peer
+// may still be reading; each pass clears the buffer the next one fills.
 // Each CTA then posts its counts of keys above and equal to the threshold to
 // every CTA: tier 1's ride on tier 2's first barrier, tier 2's take one last
 // exchange, and from them every CTA knows the members of the CTAs before it (ties
@@ -105,24 +106,6 @@ __device__ __forceinline__ int cshift(int p) { return p == 0 ? 21 : (p == 1 ? 10
 __device__ __forceinline__ uint32_t chi_mask(int p) { return p == 0 ? 0u : (p == 1 ? 0xffe00000u : 0xfffffc00u); }
 __device__ __forceinline__ uint32_t cdigit_mask(int p) { return p == 2 ? 0x3ffu : 0x7ffu; }
 
-// Exclusive CTA scan of one value per thread (returns the prefix).
-__device__ __forceinline__ uint32_t cta_scan(uint32_t v, ClSmem &sm) {
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    uint32_t wsum;
-    const uint32_t x = warp_excl(v, &wsum);
-    if (lane == 0) sm.wtot[wid] = wsum;
-    __syncthreads();
-    if (wid == 0) {
-        uint32_t all;
-        const uint32_t before = warp_excl(lane < kWarpsL ? sm.wtot[lane] : 0u, &all);
-        if (lane < kWarpsL) sm.wtot[lane] = before;
-    }
-    __syncthreads();
-    const uint32_t r = sm.wtot[wid] + x;
-    __syncthreads();
-    return r;
-}
-
 // Warp-uniform count per warp -> the sum over the warps before this one; *total = CTA sum.
 __device__ __forceinline__ uint32_t cta_warps_before(uint32_t wcount, ClSmem &sm, uint32_t *total) {
     const int warp = threadIdx.x >> 5;
@@ -148,24 +131,21 @@ __device__ __forceinline__ uint32_t cta_warps_before(uint32_t wcount, ClSmem &sm
 template <int CL, int Q>
 __device__ uint32_t cl_digits(const uint32_t (&key)[4 * Q], uint32_t cand, uint32_t k, ClSmem &sm, int &ph,
                               uint32_t *need, int *res_shift, bool *all_eq) {
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     uint32_t prefix = 0u, kr = k;
     int shift = 21;
     bool whole = false;
     for (int p = 0; p < 3; ++p) {
         shift = cshift(p);
         const uint32_t him = chi_mask(p), dm = cdigit_mask(p);
-        uint32_t *hist = sm.hist[ph & 1];
+        uint32_t *hist = sm.hist[ph & 1];  // zeroed (at the start, or during the previous pass)
         ++ph;
-        reinterpret_cast<uint2 *>(hist)[tid] = make_uint2(0u, 0u);
-        __syncthreads();
 #pragma unroll
         for (int j = 0; j < 4 * Q; ++j)
             if (((cand >> j) & 1u) && (key[j] & him) == (prefix & him)) {
                 const uint32_t bin = (key[j] >> shift) & dm;  // at most 2048 Q <= 16384 per bin: no carry
                 atomicAdd(&hist[bin >> 1], 1u << (16 * (bin & 1)));
             }
-        __syncthreads();
         cluster_sync();  // every CTA's histogram of this pass is complete and visible
         // bins 2047 - 4 tid .. 2044 - 4 tid (descending) summed over the cluster: words
         // 1023 - 2 tid (bins 2047 / 2046 in the high / low half) and 1022 - 2 tid (2045 / 2044)
@@ -179,8 +159,16 @@ __device__ uint32_t cl_digits(const uint32_t (&key)[4 * Q], uint32_t cand, uint3
             cnt[2] += v.x >> 16;
             cnt[3] += v.x & 0xffffu;
         }
+        // the other buffer, last read by the peers in the previous pass (they have all passed
+        // this pass's barrier), is cleared for the next pass
+        reinterpret_cast<uint2 *>(sm.hist[ph & 1])[tid] = make_uint2(0u, 0u);
         const uint32_t own = cnt[0] + cnt[1] + cnt[2] + cnt[3];
-        const uint32_t before = cta_scan(own, sm);
+        uint32_t wsum;
+        uint32_t before = warp_excl(own, &wsum);
+        if (lane == 0) sm.wtot[wid] = wsum;
+        __syncthreads();
+#pragma unroll
+        for (int w = 0; w < kWarpsL; ++w) before += w < wid ? sm.wtot[w] : 0u;
         if (before < kr && before + own >= kr) {  // exactly one thread
             uint32_t cum = before;
 #pragma unroll
@@ -198,7 +186,6 @@ __device__ uint32_t cl_digits(const uint32_t (&key)[4 * Q], uint32_t cand, uint3
         prefix |= sm.bc[1] << shift;
         kr = sm.bc[2];
         whole = sm.bc[3] != 0u;
-        __syncthreads();
         if (whole) break;  // the lower digits cannot change the set
     }
     *need = kr;
@@ -318,6 +305,10 @@ select_cl_kernel(const float *__restrict__ draft, const float *__restrict__ targ
 
     uint32_t dk[4 * Q], tk[4 * Q];
     load_keys_both<Q, VEC>(dk, tk, m > 0 ? ds : nullptr, f > 0 ? ts : nullptr, seg0, n);
+    // both histogram buffers start cleared; each pass clears the other one for the next
+    reinterpret_cast<uint2 *>(sm.hist[0])[tid] = make_uint2(0u, 0u);
+    reinterpret_cast<uint2 *>(sm.hist[1])[tid] = make_uint2(0u, 0u);
+    __syncthreads();
     uint32_t nmask = 0u, cmask = 0u;  // bit 4 q + e: in the context, a candidate
 #pragma unroll
     for (int q = 0; q < Q; ++q)
