@@ -21,12 +21,20 @@ constexpr int SLOT_BYTES = T * kHeadDim * 2; // 32 KiB: one K or V tile
 constexpr int HALF_BYTES = SLOT_BYTES / 2;   // 64 of the 128 columns
 constexpr long long WAIT_LIMIT_CYCLES = 4000000000LL;  // ~2 s
 
+// fp8 cache: the producer warp only requests the codes; converter warps (10-15) each turn
+// a sixth of every staged tile into a slot of a ring of FP8_KR bf16 tiles. The staging
+// (FP8_STAGES tiles of codes, 16 KiB each) takes the room of the bf16 ring's other slots.
+constexpr int FP8_CONVERTERS = 6;
+constexpr int FP8_KR = 3;
+constexpr int FP8_STAGES = 4;
+static_assert(2 * FP8_KR + FP8_STAGES <= 2 * RING, "fp8 ring and staging fit the bf16 ring's room");
+
 struct Bars {
     uint64_t q_full[2], q_empty[2];  // Q buffers (two only when the pipes share the rows)
     uint64_t kv_full[RING], kv_empty[RING];
     uint64_t s_full[2], p_full[2], o_done[2], o_empty[2];
-    uint64_t st_full[4];   // fp8 cache: the staged codes of an item have landed
-    uint64_t st_empty[4];  // fp8 cache: every converter has read the staged codes
+    uint64_t st_full[FP8_STAGES];   // fp8 cache: the staged codes of an item have landed
+    uint64_t st_empty[FP8_STAGES];  // fp8 cache: every converter has read the staged codes
     uint64_t mma_done;
     uint32_t tmem_base;
     uint32_t abort;
@@ -174,14 +182,6 @@ __device__ __forceinline__ void produce_sparse(Bars &bs, uint8_t *sRing, const C
     cp_async_wait_all();  // the drain: no copy is left in flight
     if (lane == 0) drain_q(bs, split_tiles, seg_i);
 }
-
-// fp8 cache: the producer warp only requests the codes; converter warps (10-15) each turn
-// a sixth of every staged tile into a slot of a ring of FP8_KR bf16 tiles. The staging
-// (FP8_STAGES tiles of codes, 16 KiB each) takes the room of the bf16 ring's other slots.
-constexpr int FP8_CONVERTERS = 6;
-constexpr int FP8_KR = 3;
-constexpr int FP8_STAGES = 4;
-static_assert(2 * FP8_KR + FP8_STAGES <= 2 * RING, "fp8 ring and staging fit the bf16 ring's room");
 
 // fp8 cache: part `part` of FP8_CONVERTERS of one K or V tile of E4M3 codes (128 rows of 128
 // codes, row r at r * 128) converted by the 32 lanes of a warp into the bf16 tile the TMA
