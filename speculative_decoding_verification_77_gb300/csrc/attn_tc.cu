@@ -39,8 +39,8 @@
 // rows they take alternate tiles of the same rows and each writes its own
 // partial. TMEM (512 columns): S_0, S_1, O_0, O_1, 128 columns each.
 // fp8 cache (dense, contiguous; 512 threads): the producer brings each K or
-// V tile as E4M3 codes by TMA into one of four staging buffers; warps 10-15
-// each convert a sixth of it into the bf16 ring (3 slots), fence the async
+// V tile as E4M3 codes by TMA into one of two staging buffers; warps 10-15
+// each convert a sixth of it into the bf16 ring (4 slots), fence the async
 // proxy and arrive on the slot and the staging buffer; the unit's K scale
 // joins the softmax scale and its V scale the final normalisation. Warps 8-15
 // give registers back (setmaxnreg) to the two softmax warpgroups.

@@ -25,8 +25,8 @@ constexpr long long WAIT_LIMIT_CYCLES = 4000000000LL;  // ~2 s
 // a sixth of every staged tile into a slot of a ring of FP8_KR bf16 tiles. The staging
 // (FP8_STAGES tiles of codes, 16 KiB each) takes the room of the bf16 ring's other slots.
 constexpr int FP8_CONVERTERS = 6;
-constexpr int FP8_KR = 3;
-constexpr int FP8_STAGES = 4;
+constexpr int FP8_KR = 4;
+constexpr int FP8_STAGES = 2;
 static_assert(2 * FP8_KR + FP8_STAGES <= 2 * RING, "fp8 ring and staging fit the bf16 ring's room");
 
 struct Bars {
