@@ -759,14 +759,21 @@ def codes_to_pool(kc, vc, bs, gen):
 
 
 @pytest.mark.parametrize("case", ["dense", "sparse", "paged_bs16", "sparse_paged_bs64", "g3", "ragged",
-                                  "bf16_out", "headline_sampled"])
+                                  "bf16_out", "headline_sampled", "rows128", "rows132", "empty_context"])
 def test_fp8_cache_matches_oracle(ops, case):
     """An E4M3 cache with a scale per (sequence, KV head) against the fp8 oracle on the same codes
-    and scales (the oracle is pinned to the bf16 one on the numbers the codes stand for)."""
+    and scales (the oracle is pinned to the bf16 one on the numbers the codes stand for). rows128 /
+    rows132: 128 and 132 query rows per KV head on the tensor-core kernel (alternate tiles of one
+    128-row block, then both pipes with a 4-row second block); empty_context: a sequence with no
+    cache token at all."""
     if case == "headline_sampled":
         w = W.workload(2)
         x = W.make_inputs(w)
         B, N, Hq, L = w.B, w.N, w.Hq, w.L
+    elif case in ("rows128", "rows132"):
+        Hq, Hkv = 8, 2
+        B, N, L = 2, (32 if case == "rows128" else 33), 900
+        x = small(350 + N, B=B, N=N, Hq=Hq, Hkv=Hkv, L=L, depth=6)
     else:
         Hq, Hkv = (12, 4) if case == "g3" else (8, 2)
         B, N, L = 2, 6, 1000
@@ -781,8 +788,8 @@ def test_fp8_cache_matches_oracle(ops, case):
         idx, _, _ = oracle.select(ds, ts, sink=4, window=16, top_m=64, budget=256)
         kw["idx"] = torch.from_numpy(idx).to(dev())
         okw["idx"] = torch.from_numpy(idx)
-    if case == "ragged":
-        cl = torch.tensor([L, 357], dtype=torch.int32)
+    if case in ("ragged", "empty_context"):
+        cl = torch.tensor([L, 357] if case == "ragged" else [0, L], dtype=torch.int32)
         kw["ctx_lens"] = cl.to(dev())
         okw["ctx_lens"] = cl
     dk, dv = kc.to(dev()), vc.to(dev())
