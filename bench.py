@@ -51,11 +51,11 @@ SWEEP_N = (1, 4, 16, 64, 256)
 # capture, keyed by the sha256 of the kernel sources it was taken on and the
 # workload; a changed kernel reports null.
 NCU_TRAFFIC = {
-    ("9f0f2e083f171533", "llama3-8b-layer-B4-L32k-N64-tree"): 540_638_208 + 8_667_648,
-    ("9f0f2e083f171533", "sparse-hybrid-B16-L32k-k2048-N8-chain"): 135_790_848 + 6_182_656,
-    # captured at L = 32k (1.08 GB of reads, 12.8 MB of partials written): reads scaled by 4
-    ("9f0f2e083f171533", "qwen2.5-72b-layer-B8-L128k-N32-tree"): 4 * 1_081_536_000 + 12_798_720,
-    ("9f0f2e083f171533", "tree-sweep-B8-L16k-N256-best-first"): 2_173_995_000 + 39_065_600,
+    ("66c8dfd232ad7dfe", "llama3-8b-layer-B4-L32k-N64-tree"): 540_639_232 + 8_330_496,
+    ("66c8dfd232ad7dfe", "sparse-hybrid-B16-L32k-k2048-N8-chain"): 135_813_888 + 6_277_888,
+    # captured at L = 32k (1.08 GB of reads, 13.0 MB of partials written): reads scaled by 4
+    ("66c8dfd232ad7dfe", "qwen2.5-72b-layer-B8-L128k-N32-tree"): 4 * 1_081_538_000 + 13_040_896,
+    ("66c8dfd232ad7dfe", "tree-sweep-B8-L16k-N256-best-first"): 2_173_979_000 + 39_140_096,
 }
 NCU_TRAFFIC_NOTE = {
     "qwen2.5-72b-layer-B8-L128k-N32-tree": "from an ncu capture at L=32k: K/V reads x4 (they grow with L), "

@@ -10,6 +10,14 @@ namespace {
 
 thread_local uint64_t g_launches = 0;
 
+// Clears a verify call's status word. It lets the cache kernel, launched behind it with
+// programmatic stream serialisation, start its set-up at once; that kernel waits for this
+// grid before it can record an error.
+__global__ void status_reset_kernel(uint32_t *status) {
+    griddep_launch_dependents();
+    if (threadIdx.x == 0) *status = 0u;
+}
+
 thread_local cudaEvent_t g_prof_start = nullptr;
 thread_local cudaEvent_t g_prof_stop = nullptr;
 thread_local cudaError_t g_last_cuda_error = cudaSuccess;
@@ -152,7 +160,9 @@ spec_status_t verify_common(const uint16_t *q, const uint16_t *k_cache, const ui
     a.v_scale = pg.v_scale;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (const cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s); e != cudaSuccess) return (spec_status_t)cuda_failure(e);
+    status_reset_kernel<<<1, 32, 0, s>>>(a.status);
+    count_launches(1);
+    if (const cudaError_t e = cudaGetLastError(); e != cudaSuccess) return (spec_status_t)cuda_failure(e);
     if (pg.table && sparse) {
         // the index set resolved to pool rows (checked there), at the end of the workspace;
         // the gather kernels then read the pool as one cache of row stride st

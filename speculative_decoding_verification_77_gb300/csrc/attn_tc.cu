@@ -144,6 +144,9 @@ cache_attn_tc_kernel(const VerifyArgs a, const SplitPlan p, const TcParams tp,
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // launched early behind the status word's reset kernel: wait for it before anything can
+    // record an error there (the set-up above overlaps it)
+    griddep_wait();
     const uint32_t tmem = bs.tmem_base;
 
     const int64_t g0 = plan_start(p, blockIdx.x), g1 = plan_start(p, blockIdx.x + 1);
@@ -533,8 +536,20 @@ cudaError_t launch_cache_attn_tc(const VerifyArgs &a, const SplitPlan &p, cudaSt
     });
     if (e != cudaSuccess) return e;
     if (ev0) cudaEventRecord(ev0, s);
-    kern<<<p.ctas, a.kv_fp8 && !sparse && !a.table ? THREADS_FP8 : THREADS, SMEM_BYTES, s>>>(a, p, tp, mq, mk, mv);
-    e = cudaGetLastError();
+    {  // programmatic stream serialisation: the CTAs may start while the previous kernel runs
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)p.ctas);
+        cfg.blockDim = dim3(a.kv_fp8 && !sparse && !a.table ? THREADS_FP8 : THREADS);
+        cfg.dynamicSmemBytes = SMEM_BYTES;
+        cfg.stream = s;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, a, p, tp, mq, mk, mv);
+    }
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (ev1) cudaEventRecord(ev1, s);
     count_launches(1);
     *launched = true;
