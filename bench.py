@@ -51,17 +51,18 @@ SWEEP_N = (1, 4, 16, 64, 256)
 # capture, keyed by the sha256 of the kernel sources it was taken on and the
 # workload; a changed kernel reports null.
 NCU_TRAFFIC = {
-    ("66c8dfd232ad7dfe", "llama3-8b-layer-B4-L32k-N64-tree"): 540_639_232 + 8_330_496,
-    ("66c8dfd232ad7dfe", "sparse-hybrid-B16-L32k-k2048-N8-chain"): 135_813_888 + 6_277_888,
-    # captured at L = 32k (1.08 GB of reads, 13.0 MB of partials written): reads scaled by 4
-    ("66c8dfd232ad7dfe", "qwen2.5-72b-layer-B8-L128k-N32-tree"): 4 * 1_081_538_000 + 13_040_896,
-    ("66c8dfd232ad7dfe", "tree-sweep-B8-L16k-N256-best-first"): 2_173_979_000 + 39_140_096,
+    ("0869c3ab8270ad55", "llama3-8b-layer-B4-L32k-N64-tree"): 540_684_288 + 7_547_904,
+    ("0869c3ab8270ad55", "sparse-hybrid-B16-L32k-k2048-N8-chain"): 135_795_712 + 5_921_280,
+    # captured at L = 32k (1.08 GB of reads, 11.3 MB of partials written): reads scaled by 4
+    ("0869c3ab8270ad55", "qwen2.5-72b-layer-B8-L128k-N32-tree"): 4 * 1_081_530_000 + 11_279_872,
+    ("0869c3ab8270ad55", "tree-sweep-B8-L16k-N256-best-first"): 563_206_656 + 34_059_264,
 }
 NCU_TRAFFIC_NOTE = {
     "qwen2.5-72b-layer-B8-L128k-N32-tree": "from an ncu capture at L=32k: K/V reads x4 (they grow with L), "
                                            "partial writes as captured (they do not)",
-    "tree-sweep-B8-L16k-N256-best-first": "4.1x the algorithmic bytes: G*N = 1024 rows per KV head make four "
-                                          "256-row units, each streaming the whole K/V of its head",
+    "tree-sweep-B8-L16k-N256-best-first": "G*N = 1024 rows per KV head make four 256-row units; one block of CTAs per "
+                                          "row group walks the same tiles in step, so three of every four reads of a "
+                                          "K/V tile hit L2 (1.11x the algorithmic bytes)",
 }
 
 

@@ -107,9 +107,8 @@ __global__ void __launch_bounds__(THREADS, 2) cache_attn_mma_kernel(VerifyArgs a
         const int64_t ub = u * p.tiles_per_unit;
         const int tb = (int)((g0 > ub ? g0 : ub) - ub);
         const int te = (int)((g1 < ub + p.tiles_per_unit ? g1 : ub + p.tiles_per_unit) - ub);
-        const int rg = (int)(u % p.row_groups);
-        const int hk = (int)((u / p.row_groups) % a.Hkv);
-        const int b = (int)(u / ((int64_t)p.row_groups * a.Hkv));
+        int b, hk, rg;
+        plan_unit_coords(p, a.Hkv, u, b, hk, rg);
         const int n = context_len(a, b);
         // fp8: the K scale joins the softmax scale, the V scale the partial's normalisation
         const float sl2u = FP8 ? sl2 * __ldg(a.k_scale + (int64_t)b * a.Hkv + hk) : sl2;

@@ -69,7 +69,8 @@ struct SplitPlan {
     int BM;             // query rows per unit (rows of one CTA's tile)
     int tile;           // KV positions per tile
     int row_groups;     // ceil(G*N / BM)
-    int units;          // B * Hkv * row_groups
+    int bh;             // B * Hkv
+    int units;          // B * Hkv * row_groups, row group first (plan_unit)
     int tiles_per_unit; // ceil(L_eff / tile), at least 1
     int ctas;           // CTAs of the cache kernel
     int64_t total;      // units * tiles_per_unit
@@ -154,6 +155,7 @@ inline SplitPlan make_plan(int B, int N, int Hq, int Hkv, int L_eff, int BM, int
     p.BM = BM;
     p.tile = tile;
     p.row_groups = (G * N + BM - 1) / BM;
+    p.bh = B * Hkv;
     p.units = B * Hkv * p.row_groups;
     p.tiles_per_unit = L_eff > 0 ? (L_eff + tile - 1) / tile : 1;
     p.total = (int64_t)p.units * p.tiles_per_unit;
@@ -172,9 +174,11 @@ inline SplitPlan make_plan(int B, int N, int Hq, int Hkv, int L_eff, int BM, int
 
 // Plan of the tensor-core cache kernel: units of 256 query rows (128 when G*N <= 128),
 // 128-token tiles, one CTA per SM, two pipes of 128 rows each writing their own slots.
-// Dense plans are balanced against the cost of entering a unit; sparse ones (gathered
-// tiles, where a unit switch costs less than the SMs a balanced cut leaves idle) stay
-// uniform.
+// Dense plans are balanced against the cost of entering a unit; with more than one row
+// group per (b, h_kv) and a CTA count they divide, each row group gets its own block of CTAs
+// and every block the same uniform cut (the blocks then read the same tiles in step, from L2
+// after the first); sparse plans (gathered tiles, where a unit switch costs less than the SMs
+// a balanced cut leaves idle) stay uniform.
 inline SplitPlan make_plan_tc(int B, int N, int Hq, int Hkv, int L_eff, int sms, bool sparse) {
     const int M = (Hq / Hkv) * N;
     SplitPlan p = make_plan(B, N, Hq, Hkv, L_eff, M > 128 ? 256 : 128, 128, sms);
@@ -182,8 +186,36 @@ inline SplitPlan make_plan_tc(int B, int N, int Hq, int Hkv, int L_eff, int sms,
     p.slot_rows = 128;
     p.split_tiles = M <= 128 ? 1 : 0;
     p.slots = ((int64_t)p.ctas + p.units - 1) * 2;
-    if (!sparse) plan_balance(p);
+    if (!sparse && p.row_groups > 1 && p.ctas % p.row_groups == 0 && p.ctas <= kPlanMaxCtas) {
+        // one block of CTAs per row group, the same uniform cut in every block: the CTAs of one
+        // head's row groups walk the same tiles at the same time
+        const int per = p.ctas / p.row_groups;
+        const int64_t blk = p.total / p.row_groups;
+        for (int c = 0; c < p.ctas; ++c) {
+            const int r = c / per, i = c % per;
+            const int64_t q = blk / per, rem = blk % per;
+            p.starts[c] = (int32_t)(r * blk + i * q + (i < rem ? i : rem));
+        }
+        p.starts[p.ctas] = (int32_t)p.total;
+        p.uniform = 0;
+    } else if (!sparse) {
+        plan_balance(p);
+    }
     return p;
+}
+
+// Unit numbering: u = rg * B * Hkv + b * Hkv + h_kv. The row groups of one (b, h_kv) lie B * Hkv
+// units apart, so that with one block of CTAs per row group (make_plan_tc) the CTAs that cover
+// them stream the same K/V tiles at the same time and share them through L2.
+__host__ __device__ __forceinline__ int64_t plan_unit(const SplitPlan &p, int Hkv, int b, int hk, int rg) {
+    return (int64_t)rg * p.bh + (int64_t)b * Hkv + hk;
+}
+__host__ __device__ __forceinline__ void plan_unit_coords(const SplitPlan &p, int Hkv, int64_t u, int &b, int &hk,
+                                                          int &rg) {
+    rg = (int)(u / p.bh);
+    const int bh = (int)(u - (int64_t)rg * p.bh);
+    b = bh / Hkv;
+    hk = bh - b * Hkv;
 }
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

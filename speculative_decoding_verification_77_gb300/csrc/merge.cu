@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(256) merge_tree_kernel(VerifyArgs a, SplitPlan
     griddep_wait();
     const int rfull = i * a.G + gb * GB;  // first unit row of the block (a multiple of GB)
     const int rg = rfull / p.BM, ru = rfull - rg * p.BM;
-    const int u = (b * a.Hkv + hk) * p.row_groups + rg;
+    const int u = (int)plan_unit(p, a.Hkv, b, hk, rg);
     const int h_lo = p.split_tiles ? 0 : ru / p.slot_rows;
     const int nh_shift = p.split_tiles && p.pipes == 2 ? 1 : 0;  // one or two pipe slots per CTA
     const int r = p.split_tiles ? ru : ru % p.slot_rows;

@@ -78,9 +78,7 @@ __device__ __forceinline__ void seg_decode(const VerifyArgs &a, const SplitPlan 
     s.u = u;
     s.tb = (int)((g0 > ub ? g0 : ub) - ub);
     s.te = (int)((g1 < ub + p.tiles_per_unit ? g1 : ub + p.tiles_per_unit) - ub);
-    s.rg = (int)(u % p.row_groups);
-    s.hk = (int)((u / p.row_groups) % a.Hkv);
-    s.b = (int)(u / ((int64_t)p.row_groups * a.Hkv));
+    plan_unit_coords(p, a.Hkv, u, s.b, s.hk, s.rg);
     const int nt = s.te - s.tb;
     s.cnt[0] = split_tiles ? (nt + 1) / 2 : nt;
     s.cnt[1] = split_tiles ? nt / 2 : nt;
