@@ -174,11 +174,11 @@ inline SplitPlan make_plan(int B, int N, int Hq, int Hkv, int L_eff, int BM, int
 
 // Plan of the tensor-core cache kernel: units of 256 query rows (128 when G*N <= 128),
 // 128-token tiles, one CTA per SM, two pipes of 128 rows each writing their own slots.
-// Dense plans are balanced against the cost of entering a unit; with more than one row
-// group per (b, h_kv) and a CTA count they divide, each row group gets its own block of CTAs
-// and every block the same uniform cut (the blocks then read the same tiles in step, from L2
-// after the first); sparse plans (gathered tiles, where a unit switch costs less than the SMs
-// a balanced cut leaves idle) stay uniform.
+// With more than one row group per (b, h_kv), each row group gets its own block of CTAs and
+// every block the same uniform cut (the blocks then read the same tiles in step, from L2 after
+// the first). Otherwise dense plans are balanced against the cost of entering a unit, and
+// sparse ones (gathered tiles, where a unit switch costs less than the SMs a balanced cut
+// leaves idle) stay uniform.
 inline SplitPlan make_plan_tc(int B, int N, int Hq, int Hkv, int L_eff, int sms, bool sparse) {
     const int M = (Hq / Hkv) * N;
     SplitPlan p = make_plan(B, N, Hq, Hkv, L_eff, M > 128 ? 256 : 128, 128, sms);
@@ -186,10 +186,13 @@ inline SplitPlan make_plan_tc(int B, int N, int Hq, int Hkv, int L_eff, int sms,
     p.slot_rows = 128;
     p.split_tiles = M <= 128 ? 1 : 0;
     p.slots = ((int64_t)p.ctas + p.units - 1) * 2;
-    if (!sparse && p.row_groups > 1 && p.ctas % p.row_groups == 0 && p.ctas <= kPlanMaxCtas) {
-        // one block of CTAs per row group, the same uniform cut in every block: the CTAs of one
-        // head's row groups walk the same tiles at the same time
+    if (p.row_groups > 1 && p.ctas >= p.row_groups && p.ctas <= kPlanMaxCtas) {
+        // one block of CTAs per row group (the CTAs the row groups do not divide stay idle), the
+        // same uniform cut in every block: the CTAs of one head's row groups walk the same tiles
+        // at the same time. Dense and sparse calls take the same CTA count (one workspace size).
         const int per = p.ctas / p.row_groups;
+        p.ctas = per * p.row_groups;
+        p.slots = ((int64_t)p.ctas + p.units - 1) * 2;
         const int64_t blk = p.total / p.row_groups;
         for (int c = 0; c < p.ctas; ++c) {
             const int r = c / per, i = c % per;
