@@ -51,11 +51,11 @@ SWEEP_N = (1, 4, 16, 64, 256)
 # capture, keyed by the sha256 of the kernel sources it was taken on and the
 # workload; a changed kernel reports null.
 NCU_TRAFFIC = {
-    ("0869c3ab8270ad55", "llama3-8b-layer-B4-L32k-N64-tree"): 540_684_288 + 7_547_904,
-    ("0869c3ab8270ad55", "sparse-hybrid-B16-L32k-k2048-N8-chain"): 135_795_712 + 5_921_280,
+    ("1a6c515c26ca7c5f", "llama3-8b-layer-B4-L32k-N64-tree"): 540_654_336 + 7_333_632,
+    ("1a6c515c26ca7c5f", "sparse-hybrid-B16-L32k-k2048-N8-chain"): 135_812_096 + 6_123_264,
     # captured at L = 32k (1.08 GB of reads, 11.3 MB of partials written): reads scaled by 4
-    ("0869c3ab8270ad55", "qwen2.5-72b-layer-B8-L128k-N32-tree"): 4 * 1_081_530_000 + 11_279_872,
-    ("0869c3ab8270ad55", "tree-sweep-B8-L16k-N256-best-first"): 563_206_656 + 34_059_264,
+    ("1a6c515c26ca7c5f", "qwen2.5-72b-layer-B8-L128k-N32-tree"): 4 * 1_081_574_000 + 11_319_552,
+    ("1a6c515c26ca7c5f", "tree-sweep-B8-L16k-N256-best-first"): 563_341_056 + 33_412_352,
 }
 NCU_TRAFFIC_NOTE = {
     "qwen2.5-72b-layer-B8-L128k-N32-tree": "from an ncu capture at L=32k: K/V reads x4 (they grow with L), "
