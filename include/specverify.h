@@ -103,6 +103,10 @@ const char *spec_status_string(int status);
  * Requires 1 <= budget, 0 <= sink, window, top_m, sink + window <= budget,
  * 1 <= L <= 1572864.
  * workspace: device, >= spec_select_workspace_size() bytes, 256-byte aligned.
+ * The selection kernel allows a grid launched behind it with programmatic stream
+ * serialisation to start at once; such a grid must wait for it (griddepcontrol.wait)
+ * before reading idx or count. The verify calls do: their first kernel waits, and so
+ * their set-up runs on the SMs the selection leaves free.
  */
 size_t spec_select_workspace_size(int B, int L, int budget);
 spec_status_t spec_select_topk(const float *draft_score, const float *target_score, int64_t ld,

@@ -10,11 +10,13 @@ namespace {
 
 thread_local uint64_t g_launches = 0;
 
-// Clears a verify call's status word. It lets the cache kernel, launched behind it with
-// programmatic stream serialisation, start its set-up at once; that kernel waits for this
-// grid before it can record an error.
+// Clears a verify call's status word. Launched with programmatic stream serialisation, it
+// may start while the previous grid runs (a selection lets it), so it writes only once that
+// grid is complete; it lets the cache kernel behind it start its set-up at once, and that
+// kernel waits for this grid before it can record an error or read the index set.
 __global__ void status_reset_kernel(uint32_t *status) {
     griddep_launch_dependents();
+    griddep_wait();
     if (threadIdx.x == 0) *status = 0u;
 }
 
@@ -160,7 +162,19 @@ spec_status_t verify_common(const uint16_t *q, const uint16_t *k_cache, const ui
     a.v_scale = pg.v_scale;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    status_reset_kernel<<<1, 32, 0, s>>>(a.status);
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1);
+        cfg.blockDim = dim3(32);
+        cfg.stream = s;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        if (const cudaError_t e = cudaLaunchKernelEx(&cfg, status_reset_kernel, a.status); e != cudaSuccess)
+            return (spec_status_t)cuda_failure(e);
+    }
     count_launches(1);
     if (const cudaError_t e = cudaGetLastError(); e != cudaSuccess) return (spec_status_t)cuda_failure(e);
     if (pg.table && sparse) {

@@ -277,6 +277,9 @@ select_cl_kernel(const float *__restrict__ draft, const float *__restrict__ targ
                  int32_t *__restrict__ idx, int32_t *__restrict__ count, uint32_t *status) {
     static_assert(4 * Q <= 32, "one bit per token of a thread in a 32-bit mask");
     __shared__ __align__(16) ClSmem sm;
+    // the verify call behind this selection may launch now: its kernels do their set-up on
+    // the SMs the clusters leave free and wait for this grid before they read the index set
+    griddep_launch_dependents();
     const uint32_t rank = cluster_ctarank();
     const int b = blockIdx.x / CL;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;

@@ -294,6 +294,7 @@ select_topk_kernel(const float *__restrict__ draft, const float *__restrict__ ta
                    const int32_t *__restrict__ ctx_lens, int sink, int window, int top_m, int budget,
                    int32_t *__restrict__ idx, int32_t *__restrict__ count, uint32_t *status) {
     extern __shared__ __align__(16) uint32_t dyn[];
+    griddep_launch_dependents();  // as in the cluster selection: the verify call may start its set-up
     SelectSmem &sm = *reinterpret_cast<SelectSmem *>(dyn);
     uint32_t *bits = dyn + sizeof(SelectSmem) / sizeof(uint32_t);  // [C / 32] tier membership
     const uint32_t rank = cluster_ctarank();
