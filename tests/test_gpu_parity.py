@@ -110,6 +110,40 @@ def test_workload3_sparse_hybrid(ops):
     assert_attn_close(out, lse, ro, rl, rows)
 
 
+def test_selection_and_sparse_verify_back_to_back(ops):
+    """The sparse verify's first kernel may launch while the selection runs (the selection lets
+    dependents start, the verify's kernels wait for it before they read the index set). Two
+    score sets with different selections alternate with no synchronisation in between: every
+    result must equal, bit for bit, the same pair run with a synchronisation after the
+    selection."""
+    w = W.workload(3)
+    x = W.make_inputs(w)
+    g = to_dev(x)
+    sets = [(g["draft_score"], g["target_score"]), (g["target_score"], g["draft_score"])]
+
+    def pair(s, sync):
+        idx, _ = ops.select_topk(sets[s][0], sets[s][1], sink=w.sink, window=w.window, top_m=w.top_m,
+                                 budget=w.budget)
+        if sync:
+            torch.cuda.synchronize()
+        out, lse = ops.verify_attn_sparse(g["q"], g["k_cache"], g["v_cache"], g["k_draft"], g["v_draft"],
+                                          g["parent"], idx, scale=x["scale"])
+        return idx, out, lse
+
+    ref = []
+    for s in range(2):
+        r = pair(s, True)
+        torch.cuda.synchronize()
+        ref.append(r)
+    assert not torch.equal(ref[0][0], ref[1][0])  # the two sets select different tokens
+    runs = [(i % 2, pair(i % 2, False)) for i in range(12)]
+    torch.cuda.synchronize()
+    for s, (idx, out, lse) in runs:
+        assert torch.equal(idx, ref[s][0])
+        assert torch.equal(out, ref[s][1])
+        assert torch.equal(lse, ref[s][2])
+
+
 def unit_rows(w, per_half, seed):
     """Rows covering every (b, h_kv) unit of a dense workload, per_half rows in each half of the
     unit's rows (query heads of h_kv x draft nodes, node-major): the halves are the two softmax
