@@ -531,6 +531,29 @@ def test_bad_inputs_set_the_status_word(ops):
         assert ops.read_device_status(sws) == 0
 
 
+def test_status_word_of_back_to_back_calls(ops):
+    """Calls on one workspace with no synchronisation between them: the word holds the last
+    call's verdict. Its clearing kernel may launch while the previous call's kernels run, so it
+    must wait for them: a bad tree flagged late by the previous call's merge must not survive
+    into a clean call, and a clean call must not hide the bad one after it."""
+    x = small(52, L=300, tree="chain")
+    g = to_dev(x)
+    ws = torch.zeros(1 << 24, dtype=torch.uint8, device=dev())
+    bad = g["parent"].clone()
+    bad[0, 3] = 7  # parent after the node
+    good = g["parent"]
+
+    def call(parent):
+        ops.verify_attn(g["q"], g["k_cache"], g["v_cache"], g["k_draft"], g["v_draft"], parent,
+                        scale=x["scale"], ws=ws)
+
+    for first, second, want in ((bad, good, 0), (good, bad, 5), (bad, bad, 5), (good, good, 0)):
+        for _ in range(4):
+            call(first)
+            call(second)
+        assert ops.read_device_status(ws) == want
+
+
 def test_native_kernels_ran(ops):
     before = ops.kernel_launches()
     x = small(61, L=100)
