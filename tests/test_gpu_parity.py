@@ -208,8 +208,9 @@ def test_tree_shapes(ops, tree):
     run_dense(ops, x, to_dev(x))
 
 
-# (130, 8, 2) and (70, 8, 1): three row groups per KV head and a CTA count they divide, so the
-# tensor-core kernel's plan gives each row group its own block of CTAs (the same cut in each)
+# (130, 8, 2) and (70, 8, 1): three row groups per KV head, so the tensor-core kernel's plan gives
+# each row group its own block of CTAs with the same cut (on 152 SMs, 50 CTAs a block and two SMs
+# without a CTA; on smaller problems as many CTAs as the tiles allow)
 @pytest.mark.parametrize("N,Hq,Hkv", [(300, 4, 1), (17, 16, 2), (1, 1, 1), (33, 12, 4), (130, 8, 2), (70, 8, 1)])
 def test_row_groups_and_head_ratios(ops, N, Hq, Hkv):
     x = small(5, B=1, N=N, Hq=Hq, Hkv=Hkv, L=500, depth=6)
