@@ -56,6 +56,7 @@ NCU_TRAFFIC = {
     # captured at L = 32k (1.08 GB of reads, 11.3 MB of partials written): reads scaled by 4
     ("1a6c515c26ca7c5f", "qwen2.5-72b-layer-B8-L128k-N32-tree"): 4 * 1_081_574_000 + 11_319_552,
     ("1a6c515c26ca7c5f", "tree-sweep-B8-L16k-N256-best-first"): 563_341_056 + 33_412_352,
+    ("1a6c515c26ca7c5f", "tree-sweep-B8-L16k-N1-best-first"): 537_137_664 + 3_848_448,
 }
 NCU_TRAFFIC_NOTE = {
     "qwen2.5-72b-layer-B8-L128k-N32-tree": "from an ncu capture at L=32k: K/V reads x4 (they grow with L), "
