@@ -132,6 +132,24 @@ spec_status_t spec_select_topk(const float *draft_score, const float *target_sco
  * bytes, 256-byte aligned; holds the split partials and the status word.
  */
 size_t spec_verify_workspace_size(int B, int N, int Hq, int Hkv, int d, int L_or_budget);
+
+/* The split plan the tensor-core cache kernel follows for a verify call of this shape (a
+ * read-only view of host logic: it launches nothing, needs no GPU and allocates nothing). The
+ * cache part of a call is cut into units (b, h_kv, group of BM query rows; row group first:
+ * u = rg * B * Hkv + b * Hkv + h_kv) of tiles_per_unit 128-token tiles, numbered unit by unit;
+ * CTA c covers tiles [starts[c], starts[c + 1]).
+ *
+ * L_or_budget: L for spec_verify_attn, budget for spec_verify_attn_sparse. sms: the
+ * multiprocessor count to plan for (one CTA per SM at most). sparse: nonzero for a sparse call.
+ * starts: int32 host array of max_starts entries; receives starts[0..ctas], starts[ctas] = the
+ * tile total. info: int32 host array of 8: units, tiles_per_unit, row_groups, BM (query rows per
+ * unit), split_tiles (1: the two pipes take alternate tiles of <= 128 rows), pipes (partial
+ * slots per CTA and unit), slots (partial slots of the workspace), uniform (1: an even cut).
+ * Returns the CTA count (>= 1), or -SPEC_ERR_INVALID_ARG (bad shape, NULL arrays, max_starts
+ * below ctas + 1) or -SPEC_ERR_UNSUPPORTED (a shape the verify calls refuse as too large).
+ */
+int spec_split_plan(int B, int N, int Hq, int Hkv, int L_or_budget, int sms, int sparse, int32_t *starts,
+                    int max_starts, int32_t *info);
 spec_status_t spec_verify_attn(const uint16_t *q, const uint16_t *k_cache,
                                const uint16_t *v_cache, int64_t kv_stride_b,
                                int64_t kv_stride_h, int64_t kv_stride_t,

@@ -277,6 +277,28 @@ size_t spec_verify_workspace_size(int B, int N, int Hq, int Hkv, int d, int L_or
     return verify_bytes_any(B, N, Hq, Hkv, d, L_or_budget, sizing_sms());
 }
 
+int spec_split_plan(int B, int N, int Hq, int Hkv, int L_or_budget, int sms, int sparse, int32_t *starts,
+                    int max_starts, int32_t *info) {
+    if (B < 1 || N < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || L_or_budget < 0 || sms < 1 || !starts || !info)
+        return -(int)SPEC_ERR_INVALID_ARG;
+    // the verify calls' bound on the plan's 32-bit tile numbering
+    if ((int64_t)B * Hkv * (((int64_t)(Hq / Hkv) * N + 63) / 64) * ((int64_t)L_or_budget / 64 + 1) >=
+        ((int64_t)1 << 31))
+        return -(int)SPEC_ERR_UNSUPPORTED;
+    const SplitPlan p = make_plan_tc(B, N, Hq, Hkv, L_or_budget, sms, sparse != 0);
+    if (max_starts < p.ctas + 1) return -(int)SPEC_ERR_INVALID_ARG;
+    for (int c = 0; c <= p.ctas; ++c) starts[c] = (int32_t)plan_start(p, c);
+    info[0] = p.units;
+    info[1] = p.tiles_per_unit;
+    info[2] = p.row_groups;
+    info[3] = p.BM;
+    info[4] = p.split_tiles;
+    info[5] = p.pipes;
+    info[6] = (int32_t)p.slots;
+    info[7] = p.uniform;
+    return p.ctas;
+}
+
 spec_status_t spec_verify_attn(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                                int64_t kv_stride_b, int64_t kv_stride_h, int64_t kv_stride_t,
                                const uint16_t *k_draft, const uint16_t *v_draft,

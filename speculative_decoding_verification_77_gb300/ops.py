@@ -14,6 +14,7 @@ Names mirror the C ABI (include/specverify.h):
   lse_merge              -> spec_lse_merge
   accept_commit          -> spec_accept_commit
   budget_plan            -> spec_budget_plan (host)
+  split_plan             -> spec_split_plan (host)
   importance_scores      -> spec_importance_scores
   read_device_status     -> spec_read_device_status
 """
@@ -41,6 +42,7 @@ SIGNATURES = {
     "spec_select_workspace_size": (SZ, [I, I, I]),
     "spec_select_topk": (I, [P, P, I64, I, I, P, I, I, I, I, P, P, P, SZ, P]),
     "spec_verify_workspace_size": (SZ, [I, I, I, I, I, I]),
+    "spec_split_plan": (I, [I, I, I, I, I, I, I, P, I, P]),
     "spec_verify_attn": (I, [P, P, P, I64, I64, I64, P, P, P, I, I, I, I, I, I, P, F, P, P, P, SZ, P]),
     "spec_verify_attn_sparse": (I, [P, P, P, I64, I64, I64, P, P, P, I, I, I, I, I, I, P, F, P, I,
                                     P, P, P, SZ, P]),
@@ -396,6 +398,23 @@ def importance_scores(q, k_cache, lse, heads, *, scale=None, ctx_lens=None, out=
         heads.numel(), B, N, Hq, Hkv, d, L, _ptr(ctx_lens), float(scale), _ptr(out), out.stride(0), _ptr(status),
         _stream(q)))
     return out, status
+
+
+def split_plan(B: int, N: int, Hq: int, Hkv: int, L: int, *, sms: int, sparse: bool = False) -> dict:
+    """The tensor-core cache kernel's split plan for a call of this shape on `sms` SMs (see
+    spec_split_plan; host only). L is the budget for a sparse call. Returns dict(ctas, starts,
+    units, tiles_per_unit, row_groups, BM, split_tiles, pipes, slots, uniform)."""
+    import numpy as np
+
+    lib = load_library()
+    starts = np.zeros(513, np.int32)
+    info = np.zeros(8, np.int32)
+    p = lambda a: ctypes.c_void_p(a.ctypes.data)
+    r = lib.spec_split_plan(B, N, Hq, Hkv, L, sms, 1 if sparse else 0, p(starts), starts.shape[0], p(info))
+    if r < 0:
+        raise SpecError("spec_split_plan", -r)
+    keys = ("units", "tiles_per_unit", "row_groups", "BM", "split_tiles", "pipes", "slots", "uniform")
+    return dict(ctas=int(r), starts=starts[:r + 1].tolist(), **{k: int(v) for k, v in zip(keys, info)})
 
 
 def budget_plan(marginals, n_max: int, *, t_draft: float, l_ar: float, bytes0: float, bytes_per_node: float,
