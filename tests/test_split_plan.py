@@ -125,3 +125,25 @@ def test_rejections():
         ops.split_plan(1, 1, 4, 1, 100, sms=0)
     with pytest.raises(ops.SpecError):
         ops.split_plan(1 << 20, 256, 64, 8, 1 << 20, sms=152)  # beyond the 32-bit tile numbering
+
+
+def _align(n, a=256):
+    return (n + a - 1) // a * a
+
+
+def test_workspace_holds_the_plans_partials():
+    """spec_verify_workspace_size covers the header, the plan's fp32 partial rows (o and lse, one
+    slot of 128 rows per (CTA, unit, pipe)) and the paged index scratch, for the SM count it sizes
+    for (the current device's, 160 on a machine without one), dense and sparse alike."""
+    import torch
+
+    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 160
+    lib = ops.load_library()
+    d = 128
+    for B, N, Hq, Hkv, L, _ in shape_grid():
+        ws = lib.spec_verify_workspace_size(B, N, Hq, Hkv, d, L)
+        for sparse in (False, True):
+            p = ops.split_plan(B, N, Hq, Hkv, L, sms=sms, sparse=sparse)
+            rows = p["slots"] * 128
+            need = 256 + _align(rows * d * 4) + _align(rows * 4) + _align(B * L * 4)
+            assert ws >= need, (B, N, Hq, Hkv, L, sparse, ws, need)
