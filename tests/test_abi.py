@@ -223,3 +223,28 @@ def test_binding_refuses_cpu_tensors(lib):
     for call in calls:
         with pytest.raises(ValueError, match="CUDA tensor"):
             call()
+
+
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    """The header compiles as strict C99 (a C caller needs no C++ or torch), and a C program links
+    the library and calls a host-only entry point (no GPU needed)."""
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "caller.c"
+    src.write_text('#include "specverify.h"\n'
+                   "int main(void) {\n"
+                   "    int32_t starts[600], info[8];\n"
+                   "    int ctas = spec_split_plan(4, 64, 32, 8, 32768, 152, 0, starts, 600, info);\n"
+                   "    return (ctas == 152 && starts[0] == 0 && starts[ctas] == info[0] * info[1]) ? 0 : 1;\n"
+                   "}\n")
+    libdir = os.path.join(ROOT, "speculative_decoding_verification_77_gb300")
+    exe = tmp_path / "caller"
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        str(src), "-L", libdir, "-lspecverify", f"-Wl,-rpath,{libdir}", "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    assert subprocess.run([str(exe)], timeout=60).returncode == 0
