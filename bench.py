@@ -165,10 +165,10 @@ class ClockSampler:
                 "window_s": round(t1 - t0, 3)}
 
 
-def clock_verdict(summary) -> str | None:
+def clock_rejection(summary) -> str | None:
     """Why a timed region's clock record rejects it, or None: a hardware or thermal slowdown, or SM
     clocks held well below their maximum with no reason given (a clock lock left behind). A power
-    cap keeps the measurement (it is noted in the record); no samples, no verdict."""
+    cap keeps the measurement (it is noted in the record); no samples, no rejection."""
     if not summary or not summary.get("samples"):
         return None
     bad = [r for r in summary["reasons"] if r in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")]
@@ -623,10 +623,10 @@ def run_native(args, ws_, rank, local):
     st_ev, t1, launches = timed_region()
     # a clock record showing a slowdown (or a clock held low) rejects the timed region: measure it
     # once more, every rank together, and say why in the line
-    verdict = clock_verdict(clocks.summary(t_pre, t1, clocks.peek()))
+    rejected = clock_rejection(clocks.summary(t_pre, t1, clocks.peek()))
     remeasured = None
-    if allreduce_max(ws_, 1.0 if verdict else 0.0, dev) > 0:
-        remeasured = verdict or "another rank's clock record"
+    if allreduce_max(ws_, 1.0 if rejected else 0.0, dev) > 0:
+        remeasured = rejected or "another rank's clock record"
         t_pre = time.time()
         for i in range(20):
             case.do_flush(i)

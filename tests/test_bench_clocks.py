@@ -1,4 +1,4 @@
-"""bench.py's clock record and its verdict, on the CPU with a stand-in nvidia-smi on PATH.
+"""bench.py's clock record and the check that rejects it, on the CPU with a stand-in nvidia-smi on PATH.
 
 The bench samples SM clocks and throttle reasons during the timed region. A record showing a
 hardware or thermal slowdown, or SM clocks held well below their maximum with no reason given,
@@ -41,7 +41,7 @@ def record(tmp_path, monkeypatch, sm, top, reasons):
     t0 = time.time()
     time.sleep(0.3)
     t1 = time.time()
-    early = c.summary(t0, t1, c.peek())  # while it runs, as the bench's verdict reads it
+    early = c.summary(t0, t1, c.peek())  # while it runs, as the bench's check reads it
     c.stop()
     return early, c.summary(t0, t1)
 
@@ -54,29 +54,29 @@ def test_power_capped_record_is_kept(tmp_path, monkeypatch):
     for s in (early, final):
         assert s["sm_mhz"] == 1980 and s["sm_max_mhz"] == 2070 and s["reasons"] == ["sw_power_cap"]
         assert s["samples"] >= 3 and s["window"] == "timed"
-        assert bench.clock_verdict(s) is None
+        assert bench.clock_rejection(s) is None
 
 
 def test_hardware_slowdown_rejects(tmp_path, monkeypatch):
     early, final = record(tmp_path, monkeypatch, 1400, 2070, (A, NA, NA, NA))
-    assert bench.clock_verdict(early) == "hw_slowdown" == bench.clock_verdict(final)
+    assert bench.clock_rejection(early) == "hw_slowdown" == bench.clock_rejection(final)
 
 
 def test_thermal_slowdowns_reject(tmp_path, monkeypatch):
     _, final = record(tmp_path, monkeypatch, 1500, 2070, (NA, A, A, A))
-    assert bench.clock_verdict(final) == "hw_thermal_slowdown, sw_thermal_slowdown"
+    assert bench.clock_rejection(final) == "hw_thermal_slowdown, sw_thermal_slowdown"
 
 
 def test_clock_held_low_without_reason_rejects(tmp_path, monkeypatch):
     _, final = record(tmp_path, monkeypatch, 1200, 2070, (NA, NA, NA, NA))
     assert final["reasons"] == []
-    assert bench.clock_verdict(final) == "SM clock 1200 of 2070 MHz with no reason given"
+    assert bench.clock_rejection(final) == "SM clock 1200 of 2070 MHz with no reason given"
 
 
 def test_full_clock_and_no_samples_keep_the_measurement():
-    assert bench.clock_verdict({"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 5}) is None
+    assert bench.clock_rejection({"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 5}) is None
     none = bench.ClockSampler.summary(bench.ClockSampler.__new__(bench.ClockSampler), 0.0, 1.0, [])
-    assert none["samples"] == 0 and bench.clock_verdict(none) is None
+    assert none["samples"] == 0 and bench.clock_rejection(none) is None
 
 
 def test_parse_skips_malformed_lines():

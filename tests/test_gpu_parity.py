@@ -534,7 +534,7 @@ def test_bad_inputs_set_the_status_word(ops):
 
 def test_status_word_of_back_to_back_calls(ops):
     """Calls on one workspace with no synchronisation between them: the word holds the last
-    call's verdict. Its clearing kernel may launch while the previous call's kernels run, so it
+    call's result. Its clearing kernel may launch while the previous call's kernels run, so it
     must wait for them: a bad tree flagged late by the previous call's merge must not survive
     into a clean call, and a clean call must not hide the bad one after it."""
     x = small(52, L=300, tree="chain")
